@@ -1,0 +1,106 @@
+"""Seeded synthetic inputs (PCG32 -> Box-Muller -> bf16) for tests and the bench.
+
+This module holds none of the attention or All-to-All arithmetic; it only
+produces reproducible bf16 tensors, returned as numpy ``uint16`` arrays holding
+the bf16 bit patterns. The C source (``pcg_normal.c``) documents the recipe.
+
+Workload recipe used by the tests and the bench: seed = 1000 + workload index,
+stream 1 for Q, 2 for K, 3 for V, sigma as the workload states (1 for N(0,1),
+sqrt(2) for N(0,2)).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pcg_normal.c")
+_LIB = os.path.join(_HERE, "libxsgen.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libxsgen.so`` next to its source (plain C, gcc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.xsgen_pcg32_raw.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_void_p, ctypes.c_int64]
+        lib.xsgen_pcg32_raw.restype = None
+        lib.xsgen_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+        lib.xsgen_normal_bf16.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def pcg32_raw(seed: int, stream: int, n: int, skip: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint32)
+    _load().xsgen_pcg32_raw(seed, stream, skip, out.ctypes.data, n)
+    return out
+
+
+def normal_bf16(seed: int, stream: int, shape, sigma: float = 1.0, nthreads: int = 0) -> np.ndarray:
+    """bf16 bit patterns of sigma * N(0,1), C-contiguous, dtype uint16."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint16)
+    _load().xsgen_normal_bf16(seed, stream, float(sigma), out.ctypes.data, n, nthreads)
+    return out.reshape(shape)
+
+
+def bf16_bits_to_f32(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32 (for inspection only)."""
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even float32 -> bf16 bit patterns (for building test inputs)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+# The five synthetic workloads: (B, S, H, D, P, sigma_qk, sigma_v, scale, name).
+WORKLOADS = [
+    dict(B=1, S=256, H=8, D=64, P=4, sigma_qk=1.0, sigma_v=1.0, scale=1.0 / 8.0,
+         name="small: B=1 S=256 H=8 D=64 P=4"),
+    dict(B=1, S=4096, H=24, D=128, P=8, sigma_qk=1.0, sigma_v=1.0, scale=128 ** -0.5,
+         name="DiT: B=1 S=4096 H=24 D=128 P=8"),
+    dict(B=1, S=8192, H=24, D=128, P=8, sigma_qk=1.0, sigma_v=1.0, scale=128 ** -0.5,
+         name="B=1 S=8192 H=24 D=128 P=8"),
+    dict(B=1, S=32768, H=16, D=128, P=8, sigma_qk=1.0, sigma_v=1.0, scale=128 ** -0.5,
+         name="long video DiT: B=1 S=32768 H=16 D=128 P=8"),
+    dict(B=2, S=16384, H=40, D=128, P=4, sigma_qk=2.0 ** 0.5, sigma_v=1.0, scale=128 ** -0.5,
+         name="peaked: B=2 S=16384 H=40 D=128 P=4, Q,K ~ N(0,2)"),
+]
+
+
+def workload_inputs(idx: int, nthreads: int = 0):
+    """(q, k, v) bf16 bit arrays of shape [P][B][S][H/P][D] for workload ``idx``."""
+    w = WORKLOADS[idx]
+    shape = (w["P"], w["B"], w["S"], w["H"] // w["P"], w["D"])
+    seed = 1000 + idx
+    q = normal_bf16(seed, 1, shape, w["sigma_qk"], nthreads)
+    k = normal_bf16(seed, 2, shape, w["sigma_qk"], nthreads)
+    v = normal_bf16(seed, 3, shape, w["sigma_v"], nthreads)
+    return q, k, v
+
+
+def random_inputs(seed: int, P: int, B: int, S: int, H: int, D: int, sigma_qk: float = 1.0,
+                  sigma_v: float = 1.0, nthreads: int = 0):
+    shape = (P, B, S, H // P, D)
+    return (normal_bf16(seed, 1, shape, sigma_qk, nthreads),
+            normal_bf16(seed, 2, shape, sigma_qk, nthreads),
+            normal_bf16(seed, 3, shape, sigma_v, nthreads))
