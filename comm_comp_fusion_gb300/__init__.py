@@ -1,0 +1,127 @@
+"""Python binding of libxs.so: fused non-causal attention + Ulysses All-to-All scatter.
+
+The names match the C ABI in ``include/xs.h``. This module only marshals
+arguments: every step of the path runs in the library's CUDA kernels. There is
+no fallback; if ``libxs.so`` is missing, importing the binding raises.
+
+Arguments may be torch tensors (their ``data_ptr()`` is used; the current CUDA
+stream of their device is used unless ``stream`` is given) or raw integer
+device pointers. Shapes follow the C ABI:
+
+    q, k, v  : head-partitioned     [P][B][S][H/P][D]  bf16
+    out      : sequence-partitioned [P][B][S/P][H][D]  bf16   (attn_a2a, a2a_permute)
+               head-partitioned     [P][B][S][H/P][D]  bf16   (attn)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH, build  # noqa: F401  (build is re-exported)
+
+XS_OK = 0
+XS_ERR_NULL = 1
+XS_ERR_SHAPE = 2
+XS_ERR_ALIGN = 3
+XS_ERR_UNSUPPORTED = 4
+XS_ERR_CUDA = 5
+XS_ERR_TIMEOUT = 6
+XS_ERR_ALIAS = 7
+
+STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIGN", 4: "XS_ERR_UNSUPPORTED",
+                5: "XS_ERR_CUDA", 6: "XS_ERR_TIMEOUT", 7: "XS_ERR_ALIAS"}
+
+# Every symbol include/xs.h declares.
+EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_last_error", "xs_device_status",
+           "xs_selftest_wait_timeout", "xs_version")
+
+
+class XsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libxs.so is not built ({_LIB_PATH}); run comm_comp_fusion_gb300.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.xs_attn_a2a.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.xs_attn_a2a.restype = i
+    lib.xs_attn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.xs_attn.restype = i
+    lib.xs_a2a_permute.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.xs_a2a_permute.restype = i
+    lib.xs_last_error.argtypes = []
+    lib.xs_last_error.restype = ctypes.c_char_p
+    lib.xs_device_status.argtypes = [vp, i]
+    lib.xs_device_status.restype = i
+    lib.xs_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.xs_selftest_wait_timeout.restype = i
+    lib.xs_version.argtypes = []
+    lib.xs_version.restype = i
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.xs_last_error().decode()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream, *tensors):
+    if stream is not None:
+        return stream if isinstance(stream, int) else getattr(stream, "cuda_stream", stream)
+    for t in tensors:
+        if hasattr(t, "is_cuda") and t.is_cuda:
+            import torch
+            return torch.cuda.current_stream(t.device).cuda_stream
+    return None
+
+
+def _check(status: int) -> int:
+    if status != XS_OK:
+        raise XsError(status, last_error())
+    return status
+
+
+def attn_a2a(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
+    """Fused attention + All-to-All scatter (``xs_attn_a2a``); returns the status."""
+    st = lib.xs_attn_a2a(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale),
+                         _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def attn(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
+    """Attention only, head-partitioned output (``xs_attn``); returns the status."""
+    st = lib.xs_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def a2a_permute(inp, out, B, S, H, D, P, stream=None, check=True):
+    """Standalone All-to-All layout pass (``xs_a2a_permute``); returns the status."""
+    st = lib.xs_a2a_permute(_ptr(inp), _ptr(out), B, S, H, D, P, _stream(stream, inp, out))
+    return _check(st) if check else st
+
+
+def device_status(stream=None, clear=True) -> int:
+    """``xs_device_status``: synchronises the stream and reports in-kernel wait timeouts."""
+    return lib.xs_device_status(_stream(stream), 1 if clear else 0)
+
+
+def selftest_wait_timeout(timeout_us: int = 1000, stream=None) -> int:
+    return lib.xs_selftest_wait_timeout(int(timeout_us), _stream(stream))
+
+
+def version() -> int:
+    return lib.xs_version()

@@ -1,0 +1,259 @@
+// xs_api.cpp -- the C ABI declared in include/xs.h: argument checks (done
+// before any CUDA call, so they also run on machines without a GPU), per-device
+// attributes, TMA tensor maps and kernel launches. No device memory is
+// allocated here.
+#include "../../include/xs.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "xs_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+xs_status fail(xs_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+xs_status fail_cuda(const char *what, cudaError_t e) {
+    return fail(XS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int major = 0, minor = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+xs_status current_device(int *dev, DeviceInfo *info) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (*dev < 0 || *dev >= kMaxDevices) return fail(XS_ERR_UNSUPPORTED, "device ordinal %d out of range", *dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &d = g_dev[*dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess)
+            return fail_cuda("cudaDeviceGetAttribute", e);
+        d.ready = true;
+    }
+    *info = d;
+    if (d.major != 10 || d.minor != 3)
+        return fail(XS_ERR_UNSUPPORTED, "kernels are built for sm_103a only; device %d is sm_%d%d", *dev, d.major,
+                    d.minor);
+    return XS_OK;
+}
+
+xs_status check_device_pointer(const void *ptr, int dev, const char *name) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(XS_ERR_UNSUPPORTED, "%s is not a CUDA pointer (%s)", name, cudaGetErrorName(e));
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+        return fail(XS_ERR_UNSUPPORTED, "%s must be device memory", name);
+    if (a.type == cudaMemoryTypeDevice && a.device != dev)
+        return fail(XS_ERR_UNSUPPORTED, "%s lives on device %d, current device is %d", name, a.device, dev);
+    return XS_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+// Shape rules shared by every call. `attn` adds the multiple-of-128 rule.
+xs_status check_shape(int B, int S, int H, int D, int P, bool attn, size_t *bytes) {
+    if (B < 0 || S < 0) return fail(XS_ERR_SHAPE, "B and S must be >= 0 (got B=%d S=%d)", B, S);
+    if (H < 1 || P < 1) return fail(XS_ERR_SHAPE, "H and P must be >= 1 (got H=%d P=%d)", H, P);
+    if (H % P) return fail(XS_ERR_SHAPE, "H=%d is not a multiple of P=%d", H, P);
+    if (S % P) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of P=%d", S, P);
+    if (attn && S % 128) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of 128", S);
+    if (D != 64 && D != 128) return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64 or 128)", D);
+    const unsigned long long rows = (unsigned long long)B * S * H;
+    if (rows >= (1ull << 31)) return fail(XS_ERR_SHAPE, "B*S*H=%llu rows exceeds 2^31-1", rows);
+    *bytes = (size_t)rows * D * 2;
+    if (*bytes >= (1ull << 40)) return fail(XS_ERR_SHAPE, "tensor of %zu bytes exceeds 2^40", *bytes);
+    return XS_OK;
+}
+
+bool misaligned(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+xs_status get_encoder(EncodeTiledFn *fn) {
+    static EncodeTiledFn cached = nullptr;
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!cached) return fail(XS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (%s)", cudaGetErrorName(err));
+    *fn = cached;
+    return XS_OK;
+}
+
+// Tensor map over a head-partitioned tensor [P*B][S][Hl][D] (bf16), box = 64
+// columns x 128 tokens of one head, 128-byte swizzle (the tcgen05 K-major /
+// MN-major operand layout with 128-byte rows).
+xs_status make_head_map(CUtensorMap *m, const void *ptr, int B, int S, int H, int D, int P, const char *name) {
+    EncodeTiledFn enc;
+    xs_status st = get_encoder(&enc);
+    if (st) return st;
+    const int Hl = H / P;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hl, (cuuint64_t)S, (cuuint64_t)P * (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hl * D * 2, (cuuint64_t)S * Hl * D * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(XS_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+    return XS_OK;
+}
+
+xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                         float scale, void *stream, int epi) {
+    if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
+    size_t bytes = 0;
+    xs_status st = check_shape(B, S, H, D, P, true, &bytes);
+    if (st) return st;
+    if (!std::isfinite(scale)) return fail(XS_ERR_SHAPE, "scale must be finite");
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
+        return fail(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
+    if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
+        return fail(XS_ERR_ALIAS, "out overlaps q, k or v");
+    if (bytes == 0) return XS_OK;
+
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info))) return st;
+    if ((st = check_device_pointer(q, dev, "q")) || (st = check_device_pointer(k, dev, "k")) ||
+        (st = check_device_pointer(v, dev, "v")) || (st = check_device_pointer(out, dev, "out")))
+        return st;
+
+    CUtensorMap tq, tk, tv;
+    if ((st = make_head_map(&tq, q, B, S, H, D, P, "q")) || (st = make_head_map(&tk, k, B, S, H, D, P, "k")) ||
+        (st = make_head_map(&tv, v, B, S, H, D, P, "v")))
+        return st;
+
+    xs::AttnParams p;
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.P = P;
+    p.Hl = H / P;
+    p.Sl = S / P;
+    p.n_qt = S / 128;
+    p.n_pairs = (p.n_qt + 1) / 2;
+    p.n_kv = S / 128;
+    const long long items = (long long)P * B * p.Hl * p.n_pairs;
+    if (items >= (1ll << 31)) return fail(XS_ERR_SHAPE, "too many work items (%lld)", items);
+    p.n_items = (int)items;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
+    p.out = static_cast<uint16_t *>(out);
+    const int grid = xs::attn_grid(p.n_items, info.num_sms);
+    cudaError_t e = xs::launch_attention(D, epi, tq, tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda("attention launch", e);
+    return XS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+xs_status xs_attn_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                      float scale, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1);
+}
+
+xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                  float scale, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0);
+}
+
+xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream) {
+    if (!in || !out) return fail(XS_ERR_NULL, "in and out must be non-NULL");
+    size_t bytes = 0;
+    xs_status st = check_shape(B, S, H, D, P, false, &bytes);
+    if (st) return st;
+    if (misaligned(in) || misaligned(out)) return fail(XS_ERR_ALIGN, "in and out must be 16-byte aligned");
+    if (overlaps(in, bytes, out, bytes)) return fail(XS_ERR_ALIAS, "in and out overlap");
+    if (bytes == 0) return XS_OK;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info))) return st;
+    if ((st = check_device_pointer(in, dev, "in")) || (st = check_device_pointer(out, dev, "out"))) return st;
+
+    xs::PermParams p;
+    p.rows = (uint32_t)((unsigned long long)B * S * H);
+    p.cpr_log2 = D == 128 ? 4u : 3u;
+    p.B = (uint32_t)B;
+    p.S = (uint32_t)S;
+    p.H = (uint32_t)H;
+    p.Hl = (uint32_t)(H / P);
+    p.Sl = (uint32_t)(S / P);
+    xs::fastdiv_magic(p.H, &p.mH, &p.sH);
+    xs::fastdiv_magic(p.Sl, &p.mSl, &p.sSl);
+    xs::fastdiv_magic(p.B, &p.mB, &p.sB);
+    xs::fastdiv_magic(p.Hl, &p.mHl, &p.sHl);
+    cudaError_t e = xs::launch_permute(in, out, p, info.num_sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda("permute launch", e);
+    return XS_OK;
+}
+
+const char *xs_last_error(void) { return g_last_error.c_str(); }
+
+xs_status xs_device_status(void *stream, int clear) {
+    unsigned int word = 0;
+    cudaError_t e = xs::read_device_error(&word, clear != 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda("reading the device error word", e);
+    if (word) return fail(XS_ERR_TIMEOUT, "a bounded in-kernel wait ran out (device error word 0x%08x)", word);
+    return XS_OK;
+}
+
+xs_status xs_selftest_wait_timeout(unsigned int timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 2000000u) return fail(XS_ERR_SHAPE, "timeout_us must be in 1..2000000");
+    int dev;
+    DeviceInfo info;
+    xs_status st = current_device(&dev, &info);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = xs::launch_wait_selftest(1000ull * timeout_us, s);
+    if (e != cudaSuccess) return fail_cuda("self-test launch", e);
+    unsigned int word = 0;
+    e = xs::read_device_error(&word, true, s);
+    if (e != cudaSuccess) return fail_cuda("reading the device error word", e);
+    if (word & 0x80000000u) return fail(XS_ERR_TIMEOUT, "self-test wait ran out as designed (word 0x%08x)", word);
+    return XS_OK;
+}
+
+int xs_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,534 @@
+// xs_attn.cu -- persistent, warp-specialised non-causal attention for sm_103a
+// whose epilogue writes each finished output tile either head-partitioned or
+// straight into the post-attention All-to-All layout.
+//
+// What it computes (X-Stage paper, arXiv 2607.23264v1):
+//   * section 4.3, Figure 6: a CTA owns 128 query rows of one head and walks all
+//     ceil(S/128) K/V tiles (the Q-loop); finishing the walk yields a 128 x D
+//     output tile, and successive output tiles form the outer loop;
+//   * section 4.3, Figure 7: at an output-tile boundary the role that owns O
+//     issues that tile's stores to the destination rank, then the next tile's
+//     Q-loop runs while those stores drain; no warp or SM is reserved for
+//     communication;
+//   * section 4.3, Figure 5 (d-e): the destination is the Ulysses sequence
+//     partition: token s of global head h = r*Hl + hl goes to rank r' = s / Sl.
+//
+// Softmax is computed online (running row max m, running sum l, rescaling of
+// O when m grows), in base 2 with scale*log2(e) folded into one FMA. The row
+// max used for the exponentials is only moved when the new maximum exceeds it
+// by more than 2^8 in value; otherwise the stale maximum is kept, which bounds
+// p by 256 and leaves O/l unchanged mathematically.
+//
+// Roles (512 threads, one CTA per SM, persistent over work items):
+//   warp 0      TMA producer: Q tile pair, then K_j, V_j into a 4-slot ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+//   warp 2      tensor-memory allocator
+//   warps 4-7   softmax of query tile 0 (one thread per row)
+//   warps 8-11  softmax of query tile 1
+//   warps 12-15 epilogue: O/l -> bf16 -> shared-memory transpose -> coalesced
+//               16-byte stores into the destination rows
+// Tensor memory (512 columns): S0 | S1 | O0 | O1; P_t (bf16) overwrites the
+// first half of S_t after the softmax has read it.
+//
+// Every mbarrier wait is bounded in time; if one runs out the CTA raises a
+// shared abort flag, records the site in a device error word and winds down.
+#include "xs_internal.h"
+#include "xs_ptx.cuh"
+
+namespace xs {
+
+__device__ unsigned int g_xs_error = 0;
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s; a whole call takes milliseconds
+
+enum WaitSite : uint32_t {
+    kSiteLoadQ = 0, kSiteLoadKV, kSiteMmaQ, kSiteMmaKV, kSiteMmaP, kSiteMmaOFree, kSiteSoftS,
+    kSiteSoftL, kSiteEpiO, kSiteEpiL, kSiteDrain, kSiteSelftest
+};
+
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                       uint32_t site, unsigned long long limit_ns) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1u;
+            atomicOr(&g_xs_error, 0x80000000u | (1u << site));
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                      uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, site, kWaitLimitNs);
+}
+
+// Warp-uniform bounded wait: every lane waits, then the warp agrees.
+__device__ __forceinline__ bool warp_bwait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           uint32_t site) {
+    const bool ok = bwait(bar, parity, abort_flag, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D> struct Cfg {
+    static constexpr int kNDB = D / 64;                 // 64-column (128-byte) swizzle blocks per row
+    static constexpr uint32_t kBlk = 128u * 128u;       // one swizzle block of a 128-row tile
+    static constexpr uint32_t kTile = 128u * D * 2u;    // a 128-row Q, K or V tile
+    static constexpr int kSlots = 4;                    // K/V ring slots (K and V alternate)
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffKV = kOffQ + 2 * kTile;
+    static constexpr uint32_t kOffStage = kOffKV + kSlots * kTile;
+    static constexpr uint32_t kStageWarp = 32u * 128u;  // 32 rows x 64 bf16 per epilogue warp
+    static constexpr uint32_t kOffBar = kOffStage + 4 * kStageWarp;
+    static constexpr int kNumBars = 25;
+    static constexpr uint32_t kOffL = kOffBar + 8 * 32;       // float row sums [2][128]
+    static constexpr uint32_t kOffMisc = kOffL + 2 * 128 * 4; // tmem base, abort flag
+    static constexpr uint32_t kSmemUsed = kOffMisc + 16;
+    static constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // slack to align the base to 1024
+    __host__ __device__ static constexpr uint32_t colS(int t) { return 128u * (uint32_t)t; }
+    __host__ __device__ static constexpr uint32_t colO(int t) { return 256u + (uint32_t)D * (uint32_t)t; }
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
+
+// mbarrier slots
+enum : int {
+    BQ_FULL = 0, BQ_EMPTY = 2, BKV_FULL = 4, BKV_EMPTY = 8, BS_FULL = 12, BP_FULL = 14,
+    BO_FINAL = 16, BO_FREE = 18, BL_FULL = 20, BL_EMPTY = 22, B_DRAIN = 24
+};
+
+struct Item {
+    int rb, hl, pair;
+};
+__device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
+    Item it;
+    it.pair = item % p.n_pairs;
+    const int head = item / p.n_pairs;
+    it.hl = head % p.Hl;
+    it.rb = head / p.Hl;
+    return it;
+}
+
+// Element offset of the first element of output row (rb, hl, token s).
+template <int D, int EPI>
+__device__ __forceinline__ int64_t out_row_offset(const AttnParams &p, int rb, int hl, int s) {
+    if (EPI == 0) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
+    const int b = rb % p.B, r = rb / p.B;
+    const int h = r * p.Hl + hl;
+    const int rd = s / p.Sl, sl = s - rd * p.Sl;
+    return ((((int64_t)rd * p.B + b) * p.Sl + sl) * p.H + h) * D;
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+// Hides a value from the optimiser so that it is recomputed where used instead
+// of being hoisted (and held in registers) across a loop.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+    asm volatile("" : "+r"(x));
+    return x;
+}
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+template <int D, int EPI>
+__global__ void __launch_bounds__(512, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::kOffQ, sKV = base + C::kOffKV, sStage = base + C::kOffStage;
+    const uint32_t sBar = base + C::kOffBar;
+    float *row_l = reinterpret_cast<float *>(sm + C::kOffL);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
+    volatile uint32_t *abort_flag = misc + 1;
+#define BAR(i) (sBar + 8u * (uint32_t)(i))
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR(BQ_FULL + t), 1);
+            mbar_init(BAR(BQ_EMPTY + t), 1);
+            mbar_init(BAR(BS_FULL + t), 1);
+            mbar_init(BAR(BP_FULL + t), 4);
+            mbar_init(BAR(BO_FINAL + t), 1);
+            mbar_init(BAR(BO_FREE + t), 4);
+            mbar_init(BAR(BL_FULL + t), 4);
+            mbar_init(BAR(BL_EMPTY + t), 4);
+        }
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(BAR(BKV_FULL + s), 1);
+            mbar_init(BAR(BKV_EMPTY + s), 1);
+        }
+        mbar_init(BAR(B_DRAIN), 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(misc), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const int wg = warp >> 2;
+
+    if (wg == 0) {
+        setmaxnreg_dec<40>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            uint32_t kv_it = 0, it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+                const Item w = decode_item(p, item);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    ok = bwait(BAR(BQ_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteLoadQ);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kTile);
+                    const int s0 = (2 * w.pair + t) * 128;  // past S for an absent tile: zero fill
+#pragma unroll
+                    for (int db = 0; db < C::kNDB; ++db)
+                        tma_load_4d(sQ + t * C::kTile + db * C::kBlk, &tmq, BAR(BQ_FULL + t), db * 64, w.hl, s0,
+                                    w.rb);
+                }
+                for (int j = 0; ok && j < p.n_kv; ++j) {
+                    for (int kv = 0; kv < 2; ++kv, ++kv_it) {
+                        const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u;
+                        ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(BAR(BKV_FULL + slot), C::kTile);
+                        const CUtensorMap *m = kv ? &tmv : &tmk;
+#pragma unroll
+                        for (int db = 0; db < C::kNDB; ++db)
+                            tma_load_4d(sKV + slot * C::kTile + db * C::kBlk, m, BAR(BKV_FULL + slot), db * 64,
+                                        w.hl, j * 128, w.rb);
+                    }
+                }
+            }
+            if (!ok) {  // let copies already in flight land before the CTA exits
+                const unsigned long long t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
+            constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
+            // Descriptors differ only in the start-address field (address >> 4 in
+            // the low 14 bits), so each MMA adds a compile-time offset to a base.
+            const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
+            const uint64_t dV = sdesc_sw128(0, C::kBlk, 1024);  // MN-major V, 64-column blocks kBlk apart
+            auto issue_S = [&](int t, uint32_t slot) {
+                const uint64_t qa = dK + (opaque(sQ + t * C::kTile) >> 4);
+                const uint64_t ka = dK + (opaque(sKV + slot * C::kTile) >> 4);
+                const uint32_t d = opaque(tmem + C::colS(t));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::kBlk + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_PV = [&](int t, uint32_t slot, bool acc) {
+                const uint64_t va = dV + (opaque(sKV + slot * C::kTile) >> 4);
+                const uint32_t d = opaque(tmem + C::colO(t)), a = opaque(tmem + C::colS(t));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_ts(d, a + kk * 8, va + (kk * 2048 >> 4), idO, (acc || kk > 0) ? 1u : 0u);
+            };
+            uint32_t kv_it = 0, it = 0, pph0 = 0, pph1 = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+                ok = bwait(BAR(BQ_FULL + 0), it & 1u, abort_flag, kSiteMmaQ) &&
+                     bwait(BAR(BQ_FULL + 1), it & 1u, abort_flag, kSiteMmaQ);
+                if (!ok) break;
+                uint32_t kslot = kv_it % C::kSlots;
+                ok = bwait(BAR(BKV_FULL + kslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
+                if (!ok) break;
+                ++kv_it;
+                tc_fence_after();
+                issue_S(0, kslot);
+                tc_commit(BAR(BS_FULL + 0));
+                issue_S(1, kslot);
+                tc_commit(BAR(BS_FULL + 1));
+                tc_commit(BAR(BKV_EMPTY + kslot));
+                if (p.n_kv == 1) {
+                    tc_commit(BAR(BQ_EMPTY + 0));
+                    tc_commit(BAR(BQ_EMPTY + 1));
+                }
+                for (int j = 0; j < p.n_kv; ++j) {
+                    const uint32_t vslot = kv_it % C::kSlots;
+                    ok = bwait(BAR(BKV_FULL + vslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
+                    if (!ok) break;
+                    ++kv_it;
+                    const bool more = j + 1 < p.n_kv;
+                    // ---- tile 0: O0 += P0 V_j, then S0 for the next K/V tile
+                    ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
+                    if (ok && j == 0) ok = bwait(BAR(BO_FREE + 0), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
+                    if (!ok) break;
+                    pph0 ^= 1u;
+                    tc_fence_after();
+                    issue_PV(0, vslot, j > 0);
+                    if (!more) tc_commit(BAR(BO_FINAL + 0));
+                    if (more) {
+                        kslot = kv_it % C::kSlots;
+                        ok = bwait(BAR(BKV_FULL + kslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
+                        if (!ok) break;
+                        ++kv_it;
+                        issue_S(0, kslot);
+                        tc_commit(BAR(BS_FULL + 0));
+                        if (j + 2 == p.n_kv) tc_commit(BAR(BQ_EMPTY + 0));
+                    }
+                    // ---- tile 1
+                    ok = bwait(BAR(BP_FULL + 1), pph1, abort_flag, kSiteMmaP);
+                    if (ok && j == 0) ok = bwait(BAR(BO_FREE + 1), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
+                    if (!ok) break;
+                    pph1 ^= 1u;
+                    tc_fence_after();
+                    issue_PV(1, vslot, j > 0);
+                    tc_commit(BAR(BKV_EMPTY + vslot));
+                    if (!more) tc_commit(BAR(BO_FINAL + 1));
+                    if (more) {
+                        issue_S(1, kslot);
+                        tc_commit(BAR(BS_FULL + 1));
+                        tc_commit(BAR(BKV_EMPTY + kslot));
+                        if (j + 2 == p.n_kv) tc_commit(BAR(BQ_EMPTY + 1));
+                    }
+                }
+            }
+            if (!ok) {  // wait (bounded) for MMAs in flight before tensor memory is released
+                tc_commit(BAR(B_DRAIN));
+                uint32_t dummy = 0;
+                const unsigned long long t0 = globaltimer_ns();
+                while (!mbar_try_wait(BAR(B_DRAIN), 0) && globaltimer_ns() - t0 < 200000000ull) ++dummy;
+            }
+        }
+        __syncwarp();
+    } else if (wg == 1 || wg == 2) {
+        // ------------------------------------------------------------- softmax
+        setmaxnreg_inc<184>();
+        const int t = wg - 1;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::colS(t);
+        const uint32_t tO = tmem + lane_base + C::colO(t);
+        const int row = (warp & 3) * 32 + lane;
+        const float sl2 = p.scale_log2;
+        uint32_t sph = 0, it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+            float m = 0.f, l = 0.f;
+            for (int j = 0; j < p.n_kv; ++j) {
+                ok = warp_bwait(BAR(BS_FULL + t), sph, abort_flag, kSiteSoftS);
+                if (!ok) break;
+                sph ^= 1u;
+                tc_fence_after();
+                uint32_t sa[64], sb[64];
+                tmem_ld64(tS, sa);
+                tmem_ld64(tS + 64, sb);
+#define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
+                float mx0 = SV(0), mx1 = SV(1), mx2 = SV(2), mx3 = SV(3);
+#pragma unroll
+                for (int i = 4; i < 128; i += 4) {
+                    mx0 = fmaxf(mx0, SV(i));
+                    mx1 = fmaxf(mx1, SV(i + 1));
+                    mx2 = fmaxf(mx2, SV(i + 2));
+                    mx3 = fmaxf(mx3, SV(i + 3));
+                }
+                const float mnew = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                float alpha = 1.f;
+                bool need = false;
+                if (j == 0) {
+                    m = mnew;
+                } else if (mnew > m + 8.0f) {
+                    alpha = ex2_approx(m - mnew);
+                    m = mnew;
+                    need = true;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // The commit that signalled S_t for this step also covers the
+                    // previous O_t += P V, so O_t is stable here.
+#pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                        tmem_st32(tO + c, o);
+                    }
+                    l *= alpha;
+                }
+                const float nm = -m;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                uint32_t pa[32], pb[32];
+#pragma unroll
+                for (int i = 0; i < 64; i += 2) {
+                    const float e0 = ex2_approx(fmaf(SV(2 * i), sl2, nm));
+                    const float e1 = ex2_approx(fmaf(SV(2 * i + 1), sl2, nm));
+                    const float e2 = ex2_approx(fmaf(SV(2 * i + 2), sl2, nm));
+                    const float e3 = ex2_approx(fmaf(SV(2 * i + 3), sl2, nm));
+                    a0 += e0;
+                    a1 += e1;
+                    a2 += e2;
+                    a3 += e3;
+                    uint32_t *dstp = i < 32 ? &pa[i & 31] : &pb[i & 31];
+                    dstp[0] = pack_bf16x2(e0, e1);
+                    dstp[1] = pack_bf16x2(e2, e3);
+                }
+#undef SV
+                l += (a0 + a1) + (a2 + a3);
+                tmem_st32(tS, pa);
+                tmem_st32(tS + 32, pb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
+            }
+            if (!ok) break;
+            ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
+            if (!ok) break;
+            row_l[t * 128 + row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(BL_FULL + t));
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        setmaxnreg_dec<96>();
+        const int wq = warp & 3;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const int row = wq * 32 + lane;
+        const uint32_t stage = sStage + wq * C::kStageWarp;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+            const Item w = decode_item(p, item);
+            for (int t = 0; t < 2; ++t) {
+                ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteEpiO) &&
+                     warp_bwait(BAR(BL_FULL + t), it & 1u, abort_flag, kSiteEpiL);
+                if (!ok) break;
+                const float l = row_l[t * 128 + row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(BL_EMPTY + t));
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                const int qt = 2 * w.pair + t;
+                const bool valid = qt < p.n_qt;
+                const int64_t dst = out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row);
+                const uint32_t tO = tmem + lane_base + C::colO(t);
+#pragma unroll 1
+                for (int db = 0; db < C::kNDB; ++db) {
+                    uint32_t o[64];
+                    tmem_ld64(tO + db * 64, o);
+                    if (db == C::kNDB - 1) {  // O_t fully read: the next item may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
+                    }
+                    if (!valid) continue;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t x0 = pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l);
+                        const uint32_t x1 = pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l);
+                        const uint32_t x2 = pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l);
+                        const uint32_t x3 = pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l);
+                        const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1),
+                                     "r"(x2), "r"(x3)
+                                     : "memory");
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int idx = i * 32 + lane;
+                        const int rr = idx >> 3, c = idx & 7;
+                        const uint32_t a = stage + rr * 128 + ((c ^ (rr & 7)) << 4);
+                        uint32_t y0, y1, y2, y3;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3)
+                                     : "r"(a)
+                                     : "memory");
+                        const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
+                        uint16_t *g = p.out + d + db * 64 + c * 8;
+                        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(g), "r"(y0), "r"(y1),
+                                     "r"(y2), "r"(y3)
+                                     : "memory");
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+#undef BAR
+}
+
+int attn_grid(int n_items, int num_sms) { return n_items < num_sms ? n_items : num_sms; }
+
+template <int D, int EPI>
+static cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const AttnParams &p, int grid, cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention(int D, int epi, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const AttnParams &p, int grid, cudaStream_t stream) {
+    if (D == 128) return epi ? launch_t<128, 1>(tq, tk, tv, p, grid, stream) : launch_t<128, 0>(tq, tk, tv, p, grid, stream);
+    if (D == 64) return epi ? launch_t<64, 1>(tq, tk, tv, p, grid, stream) : launch_t<64, 0>(tq, tk, tv, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ bounded-wait self-test
+
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar_storage;
+    __shared__ uint32_t abort_word;
+    const uint32_t bar = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        abort_word = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on this barrier: the wait must run out and return.
+        (void)wait_slow(bar, 0u, &abort_word, kSiteSelftest, limit_ns);
+    }
+    __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned int *value, bool clear, cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_xs_error, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (clear && *value) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_xs_error, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+}  // namespace xs

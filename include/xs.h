@@ -1,0 +1,130 @@
+/*
+ * xs.h -- C ABI of the fused attention + post-attention All-to-All library (libxs.so).
+ *
+ * What the calls compute. Source: "X-Stage: An Overlooked Pipeline Stage for
+ * Communication-Computation Overlap in DiT Inference" (arXiv 2607.23264v1).
+ *   - Section 4.3: DiT self-attention is full, non-causal softmax attention,
+ *       O = softmax(scale * Q K^T) V   per (batch, head),
+ *     computed FlashAttention-style: a CTA owns a block of 128 query rows and
+ *     walks all K/V tiles (Figure 6); finishing the walk yields one output tile.
+ *   - Section 4.3, Figure 5 (d-e): Ulysses sequence parallelism runs attention
+ *     head-partitioned and then an All-to-All restores the sequence partition.
+ *     The fused design (Figure 7) issues each finished output tile's stores to
+ *     its destination at the tile boundary and then starts the next tile.
+ *   - Section 5.3: "FA-only" (xs_attn), "A2A-only" (xs_a2a_permute), "Serial"
+ *     (xs_attn then xs_a2a_permute) and "Fused" (xs_attn_a2a) are the four
+ *     compared implementations.
+ *
+ * Ranks. P ranks are simulated as P contiguous slices of one allocation on the
+ * calling GPU, so the All-to-All is a scatter of rows into slices; nothing
+ * crosses a device boundary. Hl = H / P heads per rank, Sl = S / P tokens per rank.
+ *
+ * Layouts (row-major, elements are bf16 stored as uint16_t, D contiguous):
+ *   head-partitioned      [P][B][S][Hl][D]  rank r holds global heads r*Hl .. r*Hl+Hl-1
+ *                                            for all S tokens
+ *   sequence-partitioned  [P][B][Sl][H][D]  rank r' holds tokens r'*Sl .. r'*Sl+Sl-1
+ *                                            for all H heads, heads in ascending order
+ *   element (r,b,s,hl,d) of the first is element (r',b,s-r'*Sl,h,d) of the second,
+ *   with h = r*Hl + hl and r' = s / Sl. With P = 1 both are plain [B][S][H][D].
+ *
+ * Common rules for every compute call:
+ *   - Pointers are DEVICE pointers on the current CUDA device, 16-byte aligned,
+ *     owned and allocated by the caller. The library allocates no device memory;
+ *     it keeps only host-side state (per-device attributes).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous: they return after the kernel is enqueued.
+ *   - Arguments are checked before anything is enqueued. A violation returns a
+ *     non-zero xs_status, enqueues nothing and leaves `out` untouched;
+ *     xs_last_error() then describes it.
+ *   - Shapes: B >= 0, S >= 0 (B == 0 or S == 0 is a valid empty call that
+ *     enqueues nothing), H >= 1, P >= 1, H % P == 0, S % P == 0, S % 128 == 0,
+ *     D in {64, 128}, scale finite. Every tensor must stay below 2^40 bytes.
+ *   - `out` must not overlap q, k or v (XS_ERR_ALIAS).
+ *   - The GPU must be compute capability 10.3 (sm_103); otherwise
+ *     XS_ERR_UNSUPPORTED.
+ *   - Inside the kernels every wait is bounded in time. A wait that runs out sets
+ *     a device-side error word and the kernel returns; xs_device_status() reports
+ *     it as XS_ERR_TIMEOUT. No valid input causes this.
+ */
+#ifndef XS_H
+#define XS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    XS_OK = 0,
+    XS_ERR_NULL = 1,        /* a required pointer is NULL */
+    XS_ERR_SHAPE = 2,       /* a shape rule above is violated */
+    XS_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    XS_ERR_UNSUPPORTED = 4, /* D not in {64,128}, wrong GPU, or a pointer that is not device memory */
+    XS_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed (message in xs_last_error) */
+    XS_ERR_TIMEOUT = 6,     /* a bounded in-kernel wait ran out (reported by xs_device_status) */
+    XS_ERR_ALIAS = 7        /* out overlaps an input */
+} xs_status;
+
+/*
+ * Fused attention + All-to-All scatter (the paper's "X-Stage-Fused" variant,
+ * section 4.3, Figure 7).
+ *   q, k, v : head-partitioned [P][B][S][Hl][D] bf16, read only.
+ *   out     : sequence-partitioned [P][B][Sl][H][D] bf16, fully overwritten.
+ *   scale   : multiplies Q K^T before the softmax (usually 1/sqrt(D)).
+ * Each finished 128-row output tile of head (r, b, hl) is written straight into
+ * the slices of the ranks that own its tokens. Bit-identical to
+ * xs_a2a_permute(xs_attn(q, k, v)) for the same arguments.
+ */
+xs_status xs_attn_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H,
+                      int D, int P, float scale, void *stream);
+
+/*
+ * Attention only (the paper's "FA-only" variant, section 5.3).
+ *   q, k, v : head-partitioned [P][B][S][Hl][D] bf16.
+ *   out     : head-partitioned [P][B][S][Hl][D] bf16 (same layout as q), fully
+ *             overwritten. P only defines the layout; P = 1 is plain [B][S][H][D].
+ */
+xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                  int P, float scale, void *stream);
+
+/*
+ * Standalone post-attention All-to-All (the paper's "A2A-only" variant, and the
+ * second half of "Serial", section 5.3).
+ *   in  : head-partitioned [P][B][S][Hl][D], 16-bit elements (any payload).
+ *   out : sequence-partitioned [P][B][Sl][H][D], fully overwritten.
+ * A pure copy: out is bit-for-bit a permutation of in. Same shape rules as the
+ * attention calls except that scale does not apply and S need only satisfy
+ * S % P == 0 (no multiple-of-128 rule). in and out must not overlap.
+ */
+xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream);
+
+/* Human-readable description of the last non-OK status returned on this host
+ * thread (empty string if none). The pointer stays valid until the next call
+ * on this thread. */
+const char *xs_last_error(void);
+
+/*
+ * Synchronises `stream` and reads the device-side error word that the kernels
+ * set when a bounded wait runs out. Returns XS_OK, XS_ERR_TIMEOUT (the word is
+ * then cleared if `clear` != 0) or XS_ERR_CUDA if the synchronisation failed.
+ */
+xs_status xs_device_status(void *stream, int clear);
+
+/*
+ * Self-test of the bounded-wait path: launches one small kernel that waits on a
+ * barrier nothing will ever complete, with a limit of `timeout_us` microseconds
+ * (1 .. 2,000,000), then returns. The call synchronises `stream` and returns
+ * XS_ERR_TIMEOUT when the wait ran out as designed (XS_OK would mean it did not),
+ * leaving the device error word cleared afterwards.
+ */
+xs_status xs_selftest_wait_timeout(unsigned int timeout_us, void *stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int xs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XS_H */

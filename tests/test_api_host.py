@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def xs():
+    import __graft_entry__
+    __graft_entry__.build()
+    import comm_comp_fusion_gb300 as m
+    return m
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "xs.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(xs_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree(xs):
+    assert _declared_symbols() == sorted(xs.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(xs):
+    lib = ctypes.CDLL(xs._LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", xs._LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\S+)", out))
+    assert set(_declared_symbols()) <= exported
+
+
+def test_version(xs):
+    assert xs.version() >= 100
+
+
+# Fake but aligned, non-overlapping "device" addresses: argument checks must
+# reject the call before anything dereferences them.
+Q, K, V, O = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+GOOD = dict(B=1, S=256, H=8, D=64, P=4, scale=0.125)
+
+
+def _attn(xs, fn, q=Q, k=K, v=V, o=O, **kw):
+    a = dict(GOOD, **kw)
+    return fn(q, k, v, o, a["B"], a["S"], a["H"], a["D"], a["P"], a["scale"], check=False)
+
+
+@pytest.mark.parametrize("fn_name", ["attn_a2a", "attn"])
+def test_attention_argument_checks(xs, fn_name):
+    fn = getattr(xs, fn_name)
+    assert _attn(xs, fn, q=0) == xs.XS_ERR_NULL
+    assert _attn(xs, fn, o=0) == xs.XS_ERR_NULL
+    assert "non-NULL" in xs.last_error()
+    assert _attn(xs, fn, H=6, P=4) == xs.XS_ERR_SHAPE          # H % P
+    assert _attn(xs, fn, S=130, P=2) == xs.XS_ERR_SHAPE        # S % 128
+    assert _attn(xs, fn, S=384, P=5, H=10) == xs.XS_ERR_SHAPE  # S % P
+    assert _attn(xs, fn, H=0) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, P=0) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, B=-1) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, scale=float("nan")) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, scale=float("inf")) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, D=96) == xs.XS_ERR_UNSUPPORTED
+    assert "D=96" in xs.last_error()
+    assert _attn(xs, fn, q=Q + 8) == xs.XS_ERR_ALIGN
+    assert _attn(xs, fn, o=O + 2) == xs.XS_ERR_ALIGN
+    assert _attn(xs, fn, o=Q + 64) == xs.XS_ERR_ALIAS
+    assert _attn(xs, fn, o=V - 16) == xs.XS_ERR_ALIAS
+    assert _attn(xs, fn, B=1 << 16, S=1 << 15, H=1 << 8) == xs.XS_ERR_SHAPE  # > 2^31 rows
+    # empty calls enqueue nothing and succeed without a GPU
+    assert _attn(xs, fn, B=0) == xs.XS_OK
+    assert _attn(xs, fn, S=0) == xs.XS_OK
+
+
+def test_permute_argument_checks(xs):
+    f = lambda i=Q, o=O, B=1, S=256, H=8, D=64, P=4: xs.a2a_permute(i, o, B, S, H, D, P, check=False)
+    assert f(i=0) == xs.XS_ERR_NULL
+    assert f(H=6) == xs.XS_ERR_SHAPE
+    assert f(S=6, P=4) == xs.XS_ERR_SHAPE
+    assert f(D=32) == xs.XS_ERR_UNSUPPORTED
+    assert f(o=O + 4) == xs.XS_ERR_ALIGN
+    assert f(o=Q + 16) == xs.XS_ERR_ALIAS
+    assert f(B=0) == xs.XS_OK
+    assert f(S=4, P=2) != xs.XS_ERR_SHAPE   # no multiple-of-128 rule for the permute
+
+
+def test_selftest_rejects_bad_limit(xs):
+    assert xs.selftest_wait_timeout(0) == xs.XS_ERR_SHAPE
+    assert xs.selftest_wait_timeout(5_000_000) == xs.XS_ERR_SHAPE
+
+
+def test_valid_call_without_gpu_fails_loudly(xs):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _attn(xs, xs.attn_a2a)
+    assert st in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
+    assert xs.last_error()
+    with pytest.raises(xs.XsError):
+        xs.attn_a2a(Q, K, V, O, 1, 256, 8, 64, 4, 0.125)

@@ -1,0 +1,78 @@
+"""Helpers shared by the GPU parity tests (device transfer, running the three
+GPU paths, row sampling, the parity tolerance)."""
+import numpy as np
+
+import oracle
+import xsgen
+
+# Parity bar against the fp64 oracle on bf16 outputs (N(0,1)-style inputs).
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+SENTINEL = 0xFFFF   # a bf16 NaN pattern that a finite output can never hold
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def from_dev(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def run_paths(q, k, v, B, S, H, D, P, scale, stream=None):
+    """Returns (fused, head_partitioned, serial) outputs as uint16 arrays."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    n = P * B * S * (H // P) * D
+    fused = torch.full((n,), -1, dtype=torch.int16, device="cuda")   # sentinel 0xFFFF
+    head = torch.full_like(fused, -1)
+    serial = torch.full_like(fused, -1)
+    xs.attn_a2a(tq, tk, tv, fused, B, S, H, D, P, scale, stream=stream)
+    xs.attn(tq, tk, tv, head, B, S, H, D, P, scale, stream=stream)
+    xs.a2a_permute(head, serial, B, S, H, D, P, stream=stream)
+    torch.cuda.synchronize()
+    assert xs.device_status() == xs.XS_OK, xs.last_error()
+    return from_dev(fused), from_dev(head), from_dev(serial)
+
+
+def err_stats(got_bits, ref):
+    got = xsgen.bf16_bits_to_f32(np.asarray(got_bits)).astype(np.float64)
+    e = np.abs(got - np.asarray(ref, dtype=np.float64))
+    return float(e.max()), float(e.mean())
+
+
+def assert_close(got_bits, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what=""):
+    mx, mn = err_stats(got_bits, ref)
+    assert mx <= max_abs and mn <= mean_abs, f"{what}: max|err|={mx:.3e} mean|err|={mn:.3e}"
+    return mx, mn
+
+
+def sample_rows(B, S, H, P, n_random, seed):
+    """Head-partitioned row ids ((r*B+b)*S+s)*Hl+hl: the first and last rows of the
+    first, second and last query tiles of every head, plus random rows."""
+    Hl = H // P
+    picks = []
+    for r in range(P):
+        for b in range(B):
+            for hl in range(Hl):
+                for s in (0, 127, 128, 255, S - 128, S - 1):
+                    if 0 <= s < S:
+                        picks.append(((r * B + b) * S + s) * Hl + hl)
+    rng = np.random.default_rng(seed)
+    picks += list(rng.integers(0, P * B * S * Hl, n_random))
+    return np.unique(np.array(picks, dtype=np.int64))
+
+
+def seq_rows_of(head_rows, B, S, H, D, P):
+    """Row index, in the sequence-partitioned output, of each head-partitioned row."""
+    Hl = H // P
+    out = []
+    for row in head_rows:
+        hl = row % Hl
+        s = (row // Hl) % S
+        rb = row // (Hl * S)
+        r, b = rb // B, rb % B
+        out.append(oracle.seq_offset(b, s, r * Hl + hl, 0, B, S, H, D, P) // D)
+    return np.array(out, dtype=np.int64)
