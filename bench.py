@@ -1,0 +1,412 @@
+"""Benchmark of the fused attention + All-to-All scatter on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+A step is one xs_attn_a2a call (every step of the hot path: Q/K/V tile loads,
+QK^T, online softmax, PV, normalisation and the scatter of each output tile
+into its rank slice) over one batch of the synthetic workload. The default
+workload is the DiT-style one (B=1, S=4096, H=24, D=128, P=8); the inputs
+(PCG32 -> Box-Muller -> bf16, seed 1000 + workload index) are resident in HBM
+before timing starts. Each timed launch is preceded by a 512 MiB write that
+flushes the 129 MB L2, and timed by CUDA events recorded on the launch stream
+around that launch alone; W untimed warm-up steps come first, and the timed
+region is bracketed by a barrier and torch.cuda.synchronize().
+
+The line also reports, from a second timed region in the same run, the
+attention-only time, the serial composition (attention, then the standalone
+permute) and the permute alone, from which the overhead of the fused scatter
+over attention alone (E_res), the hiding ratio H and the speedup over serial
+follow (X-Stage paper, arXiv 2607.23264v1, section 5.3, Eq. 21). ``e2e``
+times the same call with the inputs copied in from pinned host memory and the
+output copied back inside the timed region.
+
+--impl reference times the fp64 CPU oracle (the checker of this library, not
+a tuned CPU implementation) on the host cores over a bounded sample of query
+rows of the same workload; it runs on rank 0 only.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU ("replicas only": the simulated All-to-All never leaves a GPU); the
+timed region's time is the maximum over ranks and ``value`` counts the work of
+all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused attn+A2A-scatter TFLOP/s, % BF16 dense peak, µs overhead vs attn-only"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ----------------------------------------------------------------- host helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_flops(w) -> float:
+    """Algorithmic work of one call: QK^T and PV, 2 * S * S * D each per (b, h)."""
+    return 4.0 * w["B"] * w["H"] * w["S"] * w["S"] * w["D"]
+
+
+def workload_bytes(w) -> int:
+    """Bytes of one bf16 tensor of the workload (Q, K, V or O)."""
+    return w["B"] * w["S"] * w["H"] * w["D"] * 2
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("xs_attn.cu", "xs_ptx.cuh"):
+        with open(os.path.join(ROOT, "comm_comp_fusion_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the fused kernel, from the committed ncu summary,
+    if it was taken on the current kernel source for this workload."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload_name)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[6:10]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "no samples"}
+        busy = [s for s, p in zip(sm, power) if p > 0.25 * max(power)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(busy), "power_w_max": max(power)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of `value` over ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle leg
+
+def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0):
+    """Times the fp64 oracle on about `seconds` of sampled query rows of workload w.
+    Returns (tflops, rows, wall_s, threads)."""
+    import numpy as np
+    import oracle
+    B, S, H, D, P = w["B"], w["S"], w["H"], w["D"], w["P"]
+    total_rows = P * B * S * (H // P)
+    rng = np.random.default_rng(seed)
+    threads = oracle.default_threads()
+    probe = rng.integers(0, total_rows, max(threads, 16))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], probe)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(threads, min(total_rows, len(probe) * seconds / dt)))
+    rows = rng.integers(0, total_rows, n)
+    t0 = time.perf_counter()
+    _, used = oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], rows, return_threads=True)
+    wall = time.perf_counter() - t0
+    flops = 4.0 * S * D * n
+    return flops / wall / 1e12, n, wall, used
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import xsgen
+    w = xsgen.WORKLOADS[args.workload]
+    q, k, v = xsgen.workload_inputs(args.workload)
+    # Each step is a bounded sample so that warm-up plus K steps stay within a few minutes.
+    per_step = args.ref_step_seconds or max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_rows_rate(w, q, k, v, per_step / 4, seed=100 + i)
+    rates, rows_total, wall_total, threads = [], 0, 0.0, 0
+    for i in range(args.steps):
+        r, n, wall, threads = oracle_rows_rate(w, q, k, v, per_step, seed=i)
+        rates.append(r)
+        rows_total += n
+        wall_total += wall
+    value = 4.0 * w["S"] * w["D"] * rows_total / wall_total / 1e12
+    sample = (f"{rows_total} query rows drawn uniformly from the {w['B'] * w['S'] * w['H']} rows of the workload "
+              f"over {args.steps} steps (~{per_step:.1f} s each); a row costs 4*S*D flop")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "S": w["S"], "H": w["H"], "D": w["D"], "P": w["P"],
+                   "parallelism": "replicas", "what": "fp64 CPU oracle (two-pass softmax attention per row)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU leg
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import comm_comp_fusion_gb300 as xs
+    import xsgen
+
+    w = xsgen.WORKLOADS[args.workload]
+    B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
+    nbytes = workload_bytes(w)
+    flops = workload_flops(w)
+    q_h, k_h, v_h = xsgen.workload_inputs(args.workload)
+    as_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(dev)
+    q, k, v = as_dev(q_h), as_dev(k_h), as_dev(v_h)
+    out = torch.empty(nbytes // 2, dtype=torch.int16, device=dev)
+    head = torch.empty_like(out)
+    serial = torch.empty_like(out)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    fused = lambda: xs.attn_a2a(q, k, v, out, B, S, H, D, P, scale, stream=sptr)
+    attn = lambda: xs.attn(q, k, v, head, B, S, H, D, P, scale, stream=sptr)
+    perm = lambda: xs.a2a_permute(head, serial, B, S, H, D, P, stream=sptr)
+
+    def serial_fn():
+        attn()
+        perm()
+
+    def timed(fns, steps):
+        """Per-launch CUDA-event times (ms) of each fn, L2 flushed before each, order rotated."""
+        ev = {i: [] for i in range(len(fns))}
+        for s in range(steps):
+            order = list(range(len(fns)))
+            order = order[s % len(order):] + order[:s % len(order)]
+            for i in order:
+                flush.fill_(s & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fns[i]()
+                e1.record(stream)
+                ev[i].append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return [[a.elapsed_time(b) for a, b in ev[i]] for i in range(len(fns))]
+
+    # warm-up (also builds the per-device state of the library)
+    for _ in range(args.warmup):
+        fused()
+        attn()
+        perm()
+    torch.cuda.synchronize(dev)
+    assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
+
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    time.sleep(0.1)
+
+    # ---- main timed region: K fused steps
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_fused = timed([fused], args.steps)[0]
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    gpu_launches = args.steps
+    local_ms = sum(t_fused)
+    max_ms = reduce_max(local_ms, world, dev)
+    ms_per_step = max_ms / args.steps
+    value = world * flops * args.steps / (max_ms * 1e-3) / 1e12
+
+    # ---- comparison region: attention only, serial (attention + permute), permute only
+    t_attn, t_serial, t_perm = timed([attn, serial_fn, perm], args.steps)
+    clocks = sampler.stop()
+    assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
+
+    # ---- end to end through the C ABI with host buffers
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()
+    qh, kh, vh = pin(q_h), pin(k_h), pin(v_h)
+    oh = torch.empty(out.numel(), dtype=torch.int16).pin_memory()
+    e2e_ms = []
+    for s in range(args.warmup + args.steps):
+        flush.fill_(s & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        fused()
+        oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if s >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_max = reduce_max(sum(e2e_ms), world, dev)
+    e2e_value = world * flops * args.steps / (e2e_max * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    med = lambda xs_: statistics.median(xs_)
+    tf_us, ta_us, ts_us, tp_us = (1e3 * med(t) for t in (t_fused, t_attn, t_serial, t_perm))
+    e_res = tf_us - ta_us
+    hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
+    kernel_tflops = flops / (tf_us * 1e-6) / 1e12
+    traffic = recorded_traffic(w["name"])
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": w["name"], "B": B, "S": S, "H": H, "D": D, "P": P, "scale": scale,
+            "inputs": "PCG32 -> Box-Muller -> bf16, seed 1000+workload index, streams q=1 k=2 v=3",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write",
+            "timing": "CUDA events on the launch stream around each launch; value = K * flop / sum of times",
+        },
+        "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "pct_bf16_peak_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+        "overhead_us_vs_attn_only": e_res,
+        "t_fused_us": tf_us, "t_attn_us": ta_us, "t_serial_us": ts_us, "t_permute_us": tp_us,
+        "e_res_us": e_res, "hiding_ratio": hiding, "speedup_vs_serial": ts_us / tf_us,
+        "permute": {"gbs": 2 * nbytes / (tp_us * 1e-6) / 1e9, "frac_hbm": 2 * nbytes / (tp_us * 1e-6) / 1e9 /
+                    peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128, scatter>", "achieved": kernel_tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic,
+                     "algorithmic_flop_per_launch": flops, "algorithmic_min_bytes_per_launch": 4 * nbytes},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
+                "ms_per_step": e2e_max / args.steps},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} uniformly drawn query rows of this workload in {wall:.1f} s wall (4*S*D flop per row)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=1, help="index into the five synthetic workloads")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-seconds", type=float, default=0.0,
+                    help="oracle seconds per step for --impl reference (default: sized to the run)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
