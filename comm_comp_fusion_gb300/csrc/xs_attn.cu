@@ -331,19 +331,19 @@ __global__ void __launch_bounds__(512, 1)
                 if (!ok) break;
                 sph ^= 1u;
                 tc_fence_after();
-                uint32_t sa[64], sb[64];
-                tmem_ld64(tS, sa);
-                tmem_ld64(tS + 64, sb);
-#define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
-                float mx0 = SV(0), mx1 = SV(1), mx2 = SV(2), mx3 = SV(3);
+                uint32_t s[128];
+                tmem_ld128(tS, s);
+                // row max: four chains of three-input max
+                float mx0 = fmaxf(u2f(s[0]), u2f(s[1])), mx1 = fmaxf(u2f(s[2]), u2f(s[3]));
+                float mx2 = fmaxf(u2f(s[4]), u2f(s[5])), mx3 = fmaxf(u2f(s[6]), u2f(s[7]));
 #pragma unroll
-                for (int i = 4; i < 128; i += 4) {
-                    mx0 = fmaxf(mx0, SV(i));
-                    mx1 = fmaxf(mx1, SV(i + 1));
-                    mx2 = fmaxf(mx2, SV(i + 2));
-                    mx3 = fmaxf(mx3, SV(i + 3));
+                for (int i = 8; i < 128; i += 8) {
+                    mx0 = fmax3(mx0, u2f(s[i + 0]), u2f(s[i + 1]));
+                    mx1 = fmax3(mx1, u2f(s[i + 2]), u2f(s[i + 3]));
+                    mx2 = fmax3(mx2, u2f(s[i + 4]), u2f(s[i + 5]));
+                    mx3 = fmax3(mx3, u2f(s[i + 6]), u2f(s[i + 7]));
                 }
-                const float mnew = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float mnew = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
                 float alpha = 1.f;
                 bool need = false;
                 if (j == 0) {
@@ -366,25 +366,30 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     l *= alpha;
                 }
-                const float nm = -m;
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                // p = exp2(s * scale*log2e - m): paired FMAs, ex2, paired sums, bf16 pairs
+                const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+                uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
                 uint32_t pa[32], pb[32];
 #pragma unroll
                 for (int i = 0; i < 64; i += 2) {
-                    const float e0 = ex2_approx(fmaf(SV(2 * i), sl2, nm));
-                    const float e1 = ex2_approx(fmaf(SV(2 * i + 1), sl2, nm));
-                    const float e2 = ex2_approx(fmaf(SV(2 * i + 2), sl2, nm));
-                    const float e3 = ex2_approx(fmaf(SV(2 * i + 3), sl2, nm));
-                    a0 += e0;
-                    a1 += e1;
-                    a2 += e2;
-                    a3 += e3;
+                    float e0, e1, e2, e3;
+                    f2unpack(ffma2(f2pack(u2f(s[2 * i]), u2f(s[2 * i + 1])), sc2, nm2), e0, e1);
+                    f2unpack(ffma2(f2pack(u2f(s[2 * i + 2]), u2f(s[2 * i + 3])), sc2, nm2), e2, e3);
+                    e0 = ex2_approx(e0);
+                    e1 = ex2_approx(e1);
+                    e2 = ex2_approx(e2);
+                    e3 = ex2_approx(e3);
+                    acc0 = fadd2(acc0, f2pack(e0, e1));
+                    acc1 = fadd2(acc1, f2pack(e2, e3));
                     uint32_t *dstp = i < 32 ? &pa[i & 31] : &pb[i & 31];
                     dstp[0] = pack_bf16x2(e0, e1);
                     dstp[1] = pack_bf16x2(e2, e3);
                 }
-#undef SV
-                l += (a0 + a1) + (a2 + a3);
+                {
+                    float a0, a1;
+                    f2unpack(fadd2(acc0, acc1), a0, a1);
+                    l += a0 + a1;
+                }
                 tmem_st32(tS, pa);
                 tmem_st32(tS + 32, pb);
                 tmem_st_wait();
