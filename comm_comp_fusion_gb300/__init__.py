@@ -27,13 +27,14 @@ XS_ERR_UNSUPPORTED = 4
 XS_ERR_CUDA = 5
 XS_ERR_TIMEOUT = 6
 XS_ERR_ALIAS = 7
+XS_ERR_WORKSPACE = 8
 
 STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIGN", 4: "XS_ERR_UNSUPPORTED",
-                5: "XS_ERR_CUDA", 6: "XS_ERR_TIMEOUT", 7: "XS_ERR_ALIAS"}
+                5: "XS_ERR_CUDA", 6: "XS_ERR_TIMEOUT", 7: "XS_ERR_ALIAS", 8: "XS_ERR_WORKSPACE"}
 
 # Every symbol include/xs.h declares.
-EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_last_error", "xs_device_status",
-           "xs_selftest_wait_timeout", "xs_version")
+EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size",
+           "xs_last_error", "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
 
 
 class XsError(RuntimeError):
@@ -53,6 +54,13 @@ def _load() -> ctypes.CDLL:
     lib.xs_attn.restype = i
     lib.xs_a2a_permute.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.xs_a2a_permute.restype = i
+    sz = ctypes.c_size_t
+    lib.xs_attn_a2a_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_a2a_ws.restype = i
+    lib.xs_attn_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_ws.restype = i
+    lib.xs_attn_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
+    lib.xs_attn_workspace_size.restype = i
     lib.xs_last_error.argtypes = []
     lib.xs_last_error.restype = ctypes.c_char_p
     lib.xs_device_status.argtypes = [vp, i]
@@ -106,6 +114,35 @@ def attn(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
     """Attention only, head-partitioned output (``xs_attn``); returns the status."""
     st = lib.xs_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _stream(stream, q, out))
     return _check(st) if check else st
+
+
+def _nbytes(ws, ws_bytes):
+    if ws_bytes is not None:
+        return int(ws_bytes)
+    if ws is None or isinstance(ws, int):
+        return 0
+    return ws.numel() * ws.element_size()
+
+
+def attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, workspace, workspace_bytes=None, stream=None, check=True):
+    """Fused call with the balanced schedule (``xs_attn_a2a_ws``); returns the status."""
+    st = lib.xs_attn_a2a_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                            _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def attn_ws(q, k, v, out, B, S, H, D, P, scale, workspace, workspace_bytes=None, stream=None, check=True):
+    """Attention only with the balanced schedule (``xs_attn_ws``); returns the status."""
+    st = lib.xs_attn_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                        _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def workspace_size(B, S, H, D, P) -> int:
+    """``xs_attn_workspace_size`` for the current device, in bytes."""
+    n = ctypes.c_size_t(0)
+    _check(lib.xs_attn_workspace_size(B, S, H, D, P, ctypes.byref(n)))
+    return n.value
 
 
 def a2a_permute(inp, out, B, S, H, D, P, stream=None, check=True):

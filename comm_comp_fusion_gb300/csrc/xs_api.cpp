@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -138,8 +139,10 @@ xs_status make_head_map(CUtensorMap *m, const void *ptr, int B, int S, int H, in
     return XS_OK;
 }
 
+std::atomic<uint32_t> g_generation{1};
+
 xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
-                         float scale, void *stream, int epi) {
+                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0) {
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
@@ -149,6 +152,13 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         return fail(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
     if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
         return fail(XS_ERR_ALIAS, "out overlaps q, k or v");
+    if (!ws && ws_bytes) return fail(XS_ERR_WORKSPACE, "workspace is NULL but workspace_bytes is %zu", ws_bytes);
+    if (ws) {
+        if (((uintptr_t)ws & 255u) != 0) return fail(XS_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        if (overlaps(ws, ws_bytes, q, bytes) || overlaps(ws, ws_bytes, k, bytes) || overlaps(ws, ws_bytes, v, bytes) ||
+            overlaps(ws, ws_bytes, out, bytes))
+            return fail(XS_ERR_WORKSPACE, "workspace overlaps q, k, v or out");
+    }
     if (bytes == 0) return XS_OK;
 
     int dev;
@@ -178,7 +188,20 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     p.n_items = (int)items;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
     p.out = static_cast<uint16_t *>(out);
-    const int grid = xs::attn_grid(p.n_items, info.num_sms);
+    p.ws_rec = nullptr;
+    p.ws_cnt = nullptr;
+    p.gen = 0;
+    if (ws) {
+        const size_t need = xs::attn_workspace_bytes(p.n_items, p.n_kv, D, info.num_sms);
+        if (ws_bytes < need)
+            return fail(XS_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+        if ((st = check_device_pointer(ws, dev, "workspace"))) return st;
+        const size_t rec = ((size_t)2 * info.num_sms * xs::partial_record_bytes(D) + 255) & ~(size_t)255;
+        p.ws_rec = static_cast<float *>(ws);
+        p.ws_cnt = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + rec);
+        p.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
+    }
+    const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr);
     cudaError_t e = xs::launch_attention(D, epi, tq, tk, tv, p, grid, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
     return XS_OK;
@@ -196,6 +219,33 @@ xs_status xs_attn_a2a(const void *q, const void *k, const void *v, void *out, in
 xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                   float scale, void *stream) {
     return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0);
+}
+
+xs_status xs_attn_a2a_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                         float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes);
+}
+
+xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                     float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0, workspace, workspace_bytes);
+}
+
+xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *bytes) {
+    if (!bytes) return fail(XS_ERR_NULL, "bytes must be non-NULL");
+    size_t tb = 0;
+    xs_status st = check_shape(B, S, H, D, P, true, &tb);
+    if (st) return st;
+    if (tb == 0) {
+        *bytes = 0;
+        return XS_OK;
+    }
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info))) return st;
+    const long long n_items = (long long)P * B * (H / P) * ((S / 128 + 1) / 2);
+    *bytes = xs::attn_workspace_bytes((int)n_items, S / 128, D, info.num_sms);
+    return XS_OK;
 }
 
 xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream) {

@@ -30,6 +30,14 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; P_t (bf16) overwrites the
 // first half of S_t after the softmax has read it.
 //
+// Schedule: whole items round-robin, then (when the caller passes a workspace)
+// the last one to two waves of (item, K/V tile) units split evenly over all
+// CTAs. An item cut by a range boundary is computed in pieces; each piece's
+// epilogue warp writes its unnormalised rows, row max and row sum to the
+// workspace, and the warp that arrives last for those rows merges the pieces
+// in piece order and stores the final rows, so the result does not depend on
+// which piece finishes last.
+//
 // Every mbarrier wait is bounded in time; if one runs out the CTA raises a
 // shared abort flag, records the site in a device error word and winds down.
 #include "xs_internal.h"
@@ -85,8 +93,8 @@ template <int D> struct Cfg {
     static constexpr uint32_t kStageWarp = 32u * 128u;  // 32 rows x 64 bf16 per epilogue warp
     static constexpr uint32_t kOffBar = kOffStage + 4 * kStageWarp;
     static constexpr int kNumBars = 25;
-    static constexpr uint32_t kOffL = kOffBar + 8 * 32;       // float row sums [2][128]
-    static constexpr uint32_t kOffMisc = kOffL + 2 * 128 * 4; // tmem base, abort flag
+    static constexpr uint32_t kOffL = kOffBar + 8 * 32;       // float [tile][l, m][128]
+    static constexpr uint32_t kOffMisc = kOffL + 2 * 2 * 128 * 4; // tmem base, abort flag
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
     static constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // slack to align the base to 1024
     __host__ __device__ static constexpr uint32_t colS(int t) { return 128u * (uint32_t)t; }
@@ -111,6 +119,89 @@ __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     it.hl = head % p.Hl;
     it.rb = head / p.Hl;
     return it;
+}
+
+// One stretch of work for a CTA: K/V tiles [j0, j1) of an item.
+struct Seg {
+    int item, j0, j1;
+    bool split;  // not the whole K/V range: a piece of an item
+    bool first;  // starts where this CTA's balanced range starts
+};
+struct Sched {
+    int k;
+    uint32_t u, u_begin, u_end;
+};
+// First unit of CTA c's balanced range: floor(c * U / G), in 32-bit arithmetic.
+__device__ __forceinline__ uint32_t sk_start(uint32_t c, const AttnParams &p) {
+    return c * p.sk_q + (c * p.sk_r) / gridDim.x;
+}
+// The CTA whose balanced range holds unit u (binary search on the range starts).
+__device__ __forceinline__ int sk_cta_of(uint32_t u, const AttnParams &p) {
+    uint32_t lo = 0, hi = gridDim.x - 1;  // sk_start(lo) <= u < sk_start(hi + 1)
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        if (sk_start(mid, p) <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return (int)lo;
+}
+__device__ __forceinline__ void sched_init(Sched &s, const AttnParams &p) {
+    s.k = 0;
+    s.u = s.u_begin = sk_start(blockIdx.x, p);
+    s.u_end = sk_start(blockIdx.x + 1, p);
+}
+__device__ __forceinline__ bool sched_next(Sched &s, const AttnParams &p, Seg &g) {
+    while (s.k < p.n_dp) {
+        const int item = (int)blockIdx.x + s.k * (int)gridDim.x;
+        ++s.k;
+        if (item < p.n_items) {
+            g.item = item;
+            g.j0 = 0;
+            g.j1 = p.n_kv;
+            g.split = false;
+            g.first = false;
+            return true;
+        }
+    }
+    if (s.u >= s.u_end) return false;
+    const uint32_t x = s.u / (uint32_t)p.n_kv;
+    const int j0 = (int)(s.u - x * (uint32_t)p.n_kv);
+    const uint32_t rem = s.u_end - s.u;
+    const int j1 = rem < (uint32_t)(p.n_kv - j0) ? j0 + (int)rem : p.n_kv;
+    g.item = p.sk_item0 + (int)x;
+    g.j0 = j0;
+    g.j1 = j1;
+    g.split = !(j0 == 0 && j1 == p.n_kv);
+    g.first = s.u == s.u_begin;
+    s.u += (uint32_t)(j1 - j0);
+    return true;
+}
+
+// Counts an arrival on a counter stamped with this call's generation (low 12
+// bits: arrivals, high 20: generation; a stale stamp counts as zero). Returns
+// true for the n-th arrival. The CAS loop ends after at most n retries.
+__device__ __forceinline__ bool arrive_last(uint32_t *cnt, uint32_t gen, uint32_t n) {
+    gen &= 0xFFFFFu;
+    uint32_t old = *reinterpret_cast<volatile uint32_t *>(cnt);
+    for (;;) {
+        const uint32_t cur = (old >> 12) == gen ? (old & 0xFFFu) : 0u;
+        const uint32_t prev = atomicCAS(cnt, old, (gen << 12) | (cur + 1u));
+        if (prev == old) return cur + 1u == n;
+        old = prev;
+    }
+}
+
+__device__ __forceinline__ float ld_cg(const float *ptr) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ float4 ld_cg4(const float4 *ptr) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(ptr));
+    return v;
 }
 
 // Element offset of the first element of output row (rb, hl, token s).
@@ -143,7 +234,7 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t *sm = smem_raw + (base - raw);
     const uint32_t sQ = base + C::kOffQ, sKV = base + C::kOffKV, sStage = base + C::kOffStage;
     const uint32_t sBar = base + C::kOffBar;
-    float *row_l = reinterpret_cast<float *>(sm + C::kOffL);
+    float *row_ml = reinterpret_cast<float *>(sm + C::kOffL);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
     volatile uint32_t *abort_flag = misc + 1;
 #define BAR(i) (sBar + 8u * (uint32_t)(i))
@@ -184,13 +275,16 @@ __global__ void __launch_bounds__(512, 1)
     const int wg = warp >> 2;
 
     if (wg == 0) {
-        setmaxnreg_dec<40>();
+        setmaxnreg_dec<48>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------ TMA producer
             uint32_t kv_it = 0, it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-                const Item w = decode_item(p, item);
+            Sched sch;
+            sched_init(sch, p);
+            Seg g;
+            for (; ok && sched_next(sch, p, g); ++it) {
+                const Item w = decode_item(p, g.item);
                 for (int t = 0; t < 2 && ok; ++t) {
                     ok = bwait(BAR(BQ_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteLoadQ);
                     if (!ok) break;
@@ -201,7 +295,7 @@ __global__ void __launch_bounds__(512, 1)
                         tma_load_4d(sQ + t * C::kTile + db * C::kBlk, &tmq, BAR(BQ_FULL + t), db * 64, w.hl, s0,
                                     w.rb);
                 }
-                for (int j = 0; ok && j < p.n_kv; ++j) {
+                for (int j = g.j0; ok && j < g.j1; ++j) {
                     for (int kv = 0; kv < 2; ++kv, ++kv_it) {
                         const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u;
                         ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
@@ -247,7 +341,11 @@ __global__ void __launch_bounds__(512, 1)
             };
             uint32_t kv_it = 0, it = 0, pph0 = 0, pph1 = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+            Sched sch;
+            sched_init(sch, p);
+            Seg g;
+            for (; ok && sched_next(sch, p, g); ++it) {
+                const int nseg = g.j1 - g.j0;
                 ok = bwait(BAR(BQ_FULL + 0), it & 1u, abort_flag, kSiteMmaQ) &&
                      bwait(BAR(BQ_FULL + 1), it & 1u, abort_flag, kSiteMmaQ);
                 if (!ok) break;
@@ -261,16 +359,16 @@ __global__ void __launch_bounds__(512, 1)
                 issue_S(1, kslot);
                 tc_commit(BAR(BS_FULL + 1));
                 tc_commit(BAR(BKV_EMPTY + kslot));
-                if (p.n_kv == 1) {
+                if (nseg == 1) {
                     tc_commit(BAR(BQ_EMPTY + 0));
                     tc_commit(BAR(BQ_EMPTY + 1));
                 }
-                for (int j = 0; j < p.n_kv; ++j) {
+                for (int j = 0; j < nseg; ++j) {
                     const uint32_t vslot = kv_it % C::kSlots;
                     ok = bwait(BAR(BKV_FULL + vslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
                     if (!ok) break;
                     ++kv_it;
-                    const bool more = j + 1 < p.n_kv;
+                    const bool more = j + 1 < nseg;
                     // ---- tile 0: O0 += P0 V_j, then S0 for the next K/V tile
                     ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
                     if (ok && j == 0) ok = bwait(BAR(BO_FREE + 0), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
@@ -286,7 +384,7 @@ __global__ void __launch_bounds__(512, 1)
                         ++kv_it;
                         issue_S(0, kslot);
                         tc_commit(BAR(BS_FULL + 0));
-                        if (j + 2 == p.n_kv) tc_commit(BAR(BQ_EMPTY + 0));
+                        if (j + 2 == nseg) tc_commit(BAR(BQ_EMPTY + 0));
                     }
                     // ---- tile 1
                     ok = bwait(BAR(BP_FULL + 1), pph1, abort_flag, kSiteMmaP);
@@ -301,7 +399,7 @@ __global__ void __launch_bounds__(512, 1)
                         issue_S(1, kslot);
                         tc_commit(BAR(BS_FULL + 1));
                         tc_commit(BAR(BKV_EMPTY + kslot));
-                        if (j + 2 == p.n_kv) tc_commit(BAR(BQ_EMPTY + 1));
+                        if (j + 2 == nseg) tc_commit(BAR(BQ_EMPTY + 1));
                     }
                 }
             }
@@ -315,7 +413,7 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
     } else if (wg == 1 || wg == 2) {
         // ------------------------------------------------------------- softmax
-        setmaxnreg_inc<184>();
+        setmaxnreg_inc<176>();
         const int t = wg - 1;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::colS(t);
@@ -324,9 +422,13 @@ __global__ void __launch_bounds__(512, 1)
         const float sl2 = p.scale_log2;
         uint32_t sph = 0, it = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+        Sched sch;
+        sched_init(sch, p);
+        Seg g;
+        for (; ok && sched_next(sch, p, g); ++it) {
             float m = 0.f, l = 0.f;
-            for (int j = 0; j < p.n_kv; ++j) {
+            const int nseg = g.j1 - g.j0;
+            for (int j = 0; j < nseg; ++j) {
                 ok = warp_bwait(BAR(BS_FULL + t), sph, abort_flag, kSiteSoftS);
                 if (!ok) break;
                 sph ^= 1u;
@@ -400,74 +502,219 @@ __global__ void __launch_bounds__(512, 1)
             if (!ok) break;
             ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
             if (!ok) break;
-            row_l[t * 128 + row] = l;
+            row_ml[t * 256 + row] = l;
+            row_ml[t * 256 + 128 + row] = m;
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(BL_FULL + t));
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        setmaxnreg_dec<96>();
+        setmaxnreg_dec<112>();
         const int wq = warp & 3;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const int row = wq * 32 + lane;
         const uint32_t stage = sStage + wq * C::kStageWarp;
+        constexpr size_t kRecFloats = 2 * 128 * D + 2 * 2 * 128;
+        // Output rows go through shared memory: each lane writes 16-byte chunk c
+        // (8 bf16) of its own row into staging row `lane` (XOR-swizzled), then
+        // the warp copies its 32 rows out with coalesced 16-byte stores.
+        auto stage_chunk = [&](int c, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+            const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1), "r"(x2), "r"(x3)
+                         : "memory");
+        };
+        auto flush_block = [&](int64_t dst, int db) {
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int idx = i * 32 + lane;
+                const int rr = idx >> 3, c = idx & 7;
+                const uint32_t a = stage + rr * 128 + ((c ^ (rr & 7)) << 4);
+                uint32_t y0, y1, y2, y3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3)
+                             : "r"(a)
+                             : "memory");
+                const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
+                uint16_t *gp = p.out + d + db * 64 + c * 8;
+                asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gp), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+                             : "memory");
+            }
+            __syncwarp();
+        };
+        // Merge of a split item's pieces for this warp's 32 rows of tile t, in
+        // piece order. With self_tmem the piece computed by this CTA is read from
+        // tensor memory (it never went to the workspace); otherwise every piece,
+        // this CTA's included, comes from the workspace. Both read the same bits,
+        // so the result does not depend on which piece merges.
+        auto merge = [&](int t, int c_first, int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
+                         uint32_t tO, int64_t dst, bool valid) {
+            auto piece = [&](int c) -> const float * {
+                const int slot = 2 * c + (sk_start((uint32_t)c, p) >= ua ? 0 : 1);
+                return p.ws_rec + (size_t)slot * kRecFloats;
+            };
+            const int self = (int)blockIdx.x;
+            float M = -INFINITY;
+            for (int c = c_first; c <= c_last; ++c)
+                M = fmaxf(M, (self_tmem && c == self) ? m_self : ld_cg(piece(c) + 2 * 128 * D + t * 256 + row));
+            float L = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+                float mc, lc;
+                if (self_tmem && c == self) {
+                    mc = m_self;
+                    lc = l_self;
+                } else {
+                    const float *r = piece(c) + 2 * 128 * D + t * 256;
+                    mc = ld_cg(r + row);
+                    lc = ld_cg(r + 128 + row);
+                }
+                L += ex2_approx(mc - M) * lc;
+            }
+            const float inv_L = 1.0f / L;
+#pragma unroll 1
+            for (int db = 0; db < C::kNDB; ++db) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int col = db * 64 + h * 32;
+                    float acc[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                    for (int c = c_first; c <= c_last; ++c) {
+                        if (self_tmem && c == self) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + col, o);
+                            const float wk = ex2_approx(m_self - M);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) acc[i] = fmaf(wk, u2f(o[i]), acc[i]);
+                        } else {
+                            const float *r = piece(c);
+                            const float wk = ex2_approx(ld_cg(r + 2 * 128 * D + t * 256 + row) - M);
+                            const float4 *src = reinterpret_cast<const float4 *>(r) + (size_t)t * (D / 4) * 128;
+                            float4 v[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) v[q] = ld_cg4(src + (size_t)(col / 4 + q) * 128 + row);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                acc[4 * q] = fmaf(wk, v[q].x, acc[4 * q]);
+                                acc[4 * q + 1] = fmaf(wk, v[q].y, acc[4 * q + 1]);
+                                acc[4 * q + 2] = fmaf(wk, v[q].z, acc[4 * q + 2]);
+                                acc[4 * q + 3] = fmaf(wk, v[q].w, acc[4 * q + 3]);
+                            }
+                        }
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            stage_chunk(4 * h + c, pack_bf16x2(acc[8 * c + 0] * inv_L, acc[8 * c + 1] * inv_L),
+                                        pack_bf16x2(acc[8 * c + 2] * inv_L, acc[8 * c + 3] * inv_L),
+                                        pack_bf16x2(acc[8 * c + 4] * inv_L, acc[8 * c + 5] * inv_L),
+                                        pack_bf16x2(acc[8 * c + 6] * inv_L, acc[8 * c + 7] * inv_L));
+                    }
+                }
+                if (valid) flush_block(dst, db);
+            }
+        };
         uint32_t it = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-            const Item w = decode_item(p, item);
+        Sched sch;
+        sched_init(sch, p);
+        Seg g;
+        for (; ok && sched_next(sch, p, g); ++it) {
+            const Item w = decode_item(p, g.item);
+            // a split item: which CTAs hold its pieces, and this CTA's record
+            const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
+            const uint32_t ua = x_local * (uint32_t)p.n_kv;  // the item's first unit
+            int c_first = 0, c_last = 0;
+            if (g.split) {
+                c_first = sk_cta_of(ua, p);
+                c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
+            }
+            const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
+            uint32_t pending = 0;  // tiles whose partial went to the workspace
             for (int t = 0; t < 2; ++t) {
                 ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteEpiO) &&
                      warp_bwait(BAR(BL_FULL + t), it & 1u, abort_flag, kSiteEpiL);
                 if (!ok) break;
-                const float l = row_l[t * 128 + row];
+                const float l = row_ml[t * 256 + row];
+                const float m = row_ml[t * 256 + 128 + row];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(BL_EMPTY + t));
                 tc_fence_after();
-                const float inv_l = 1.0f / l;
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
                 const int64_t dst = out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row);
                 const uint32_t tO = tmem + lane_base + C::colO(t);
+                auto release_o = [&]() {  // O_t fully read: the next item may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
+                };
+                if (!g.split) {
+                    const float inv_l = 1.0f / l;
 #pragma unroll 1
-                for (int db = 0; db < C::kNDB; ++db) {
-                    uint32_t o[64];
-                    tmem_ld64(tO + db * 64, o);
-                    if (db == C::kNDB - 1) {  // O_t fully read: the next item may overwrite it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
-                    }
-                    if (!valid) continue;
+                    for (int db = 0; db < C::kNDB; ++db) {
+                        uint32_t o[64];
+                        tmem_ld64(tO + db * 64, o);
+                        if (db == C::kNDB - 1) release_o();
+                        if (!valid) continue;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t x0 = pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l);
-                        const uint32_t x1 = pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l);
-                        const uint32_t x2 = pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l);
-                        const uint32_t x3 = pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l);
-                        const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1),
-                                     "r"(x2), "r"(x3)
-                                     : "memory");
+                        for (int c = 0; c < 8; ++c)
+                            stage_chunk(c, pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
+                                        pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
+                                        pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
+                                        pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
+                        flush_block(dst, db);
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int idx = i * 32 + lane;
-                        const int rr = idx >> 3, c = idx & 7;
-                        const uint32_t a = stage + rr * 128 + ((c ^ (rr & 7)) << 4);
-                        uint32_t y0, y1, y2, y3;
-                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3)
-                                     : "r"(a)
-                                     : "memory");
-                        const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
-                        uint16_t *g = p.out + d + db * 64 + c * 8;
-                        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(g), "r"(y0), "r"(y1),
-                                     "r"(y2), "r"(y3)
-                                     : "memory");
-                    }
-                    __syncwarp();
+                    continue;
                 }
+                // ---- a piece of a split item. If every other piece has already
+                // arrived, merge now, reading this piece straight from TMEM.
+                uint32_t *cnt = p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq);
+                uint32_t others = 0;
+                if (lane == 0) {
+                    const uint32_t v = *reinterpret_cast<volatile uint32_t *>(cnt);
+                    others = ((v >> 12) == (p.gen & 0xFFFFFu) && (v & 0xFFFu) == npieces - 1u) ? 1u : 0u;
+                }
+                others = __shfl_sync(0xffffffffu, others, 0);
+                if (others) {
+                    __threadfence();
+                    merge(t, c_first, c_last, ua, true, m, l, tO, dst, valid);
+                    release_o();
+                    continue;
+                }
+                // otherwise publish this piece's rows: unnormalised O, row max, row sum
+                const int own_slot = 2 * (int)blockIdx.x + (g.first ? 0 : 1);
+                float *rec = p.ws_rec + (size_t)own_slot * kRecFloats;
+                float4 *o4 = reinterpret_cast<float4 *>(rec) + (size_t)t * (D / 4) * 128;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    if (c + 32 == D) release_o();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        o4[(size_t)(c / 4 + q) * 128 + row] =
+                            make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]), u2f(o[4 * q + 3]));
+                }
+                rec[2 * 128 * D + t * 256 + row] = m;
+                rec[2 * 128 * D + t * 256 + 128 + row] = l;
+                pending |= 1u << t;
+            }
+            if (!ok || !pending) continue;
+            // ---- count this piece's arrival for the published tiles; the last arrival merges
+            __threadfence();
+            __syncwarp();
+            for (int t = 0; t < 2; ++t) {
+                if (!(pending & (1u << t))) continue;
+                uint32_t last = 0;
+                if (lane == 0)
+                    last = arrive_last(p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq), p.gen, npieces) ? 1u : 0u;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) continue;
+                __threadfence();
+                const int qt = 2 * w.pair + t;
+                merge(t, c_first, c_last, ua, false, 0.f, 0.f, 0u,
+                      out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
             }
         }
     }
@@ -481,7 +728,44 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-int attn_grid(int n_items, int num_sms) { return n_items < num_sms ? n_items : num_sms; }
+int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
+    const long long units = (long long)p.n_items * p.n_kv;
+    p.sk_item0 = p.n_items;
+    p.sk_units = 0;
+    p.sk_q = 0;
+    p.sk_r = 0;
+    if (!balanced) {
+        const int G = p.n_items < num_sms ? p.n_items : num_sms;
+        p.n_dp = (p.n_items + G - 1) / G;
+        return G;
+    }
+    const int G = units < num_sms ? (int)units : num_sms;
+    if (p.n_items % G == 0) {
+        p.n_dp = p.n_items / G;
+        return G;
+    }
+    // keep one full wave (plus the remainder) for the balanced region
+    p.n_dp = p.n_items / G - 1;
+    if (p.n_dp < 0) p.n_dp = 0;
+    p.sk_item0 = p.n_dp * G;
+    const long long u = (long long)(p.n_items - p.sk_item0) * p.n_kv;
+    if (u >= (1ll << 31)) {  // too long to split in 32-bit arithmetic: whole items only
+        p.n_dp = (p.n_items + G - 1) / G;
+        p.sk_item0 = p.n_items;
+        return G;
+    }
+    p.sk_units = (uint32_t)u;
+    p.sk_q = p.sk_units / (uint32_t)G;
+    p.sk_r = p.sk_units % (uint32_t)G;
+    return G;
+}
+
+size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
+    (void)n_kv;
+    const size_t rec = ((size_t)2 * num_sms * partial_record_bytes(D) + 255) & ~(size_t)255;
+    const size_t cnt = ((size_t)n_items * 8 * sizeof(uint32_t) + 255) & ~(size_t)255;
+    return rec + cnt;
+}
 
 template <int D, int EPI>
 static cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -10,7 +10,14 @@ namespace xs {
 
 // Work decomposition of one attention call. A work item is a pair of
 // consecutive 128-row query tiles of one (rank, batch, local head); the second
-// tile of the last pair is absent when S/128 is odd.
+// tile of the last pair is absent when S/128 is odd. A unit is one item and
+// one 128-row K/V tile.
+//
+// Schedule: CTA c first takes whole items c, c + G, ..., c + (n_dp - 1) G
+// (G = gridDim.x). The remaining items, the "balanced region" starting at
+// sk_item0, hold sk_units units that are dealt out as G contiguous ranges of
+// equal length, [c*U/G, (c+1)*U/G); an item whose units fall into several
+// ranges is computed in pieces whose partial results meet in the workspace.
 struct AttnParams {
     int B, S, H, P, Hl, Sl;
     int n_qt;     // 128-row query tiles per head  (S / 128)
@@ -19,10 +26,24 @@ struct AttnParams {
     int n_items;  // P * B * Hl * n_pairs
     float scale_log2;  // scale * log2(e): softmax runs in base 2
     uint16_t *out;
+    int n_dp;              // round-robin waves of whole items
+    int sk_item0;          // first item of the balanced region
+    uint32_t sk_units;     // units U in the balanced region (0: none), below 2^31
+    uint32_t sk_q, sk_r;   // U = sk_q * G + sk_r, so range starts are c*q + (c*r)/G
+    float *ws_rec;         // 2 * G partial records (see partial_record_bytes)
+    uint32_t *ws_cnt;      // 8 arrival counters per item of the balanced region
+    uint32_t gen;          // generation stamped into the counters by this call
 };
 
-// Grid for the persistent attention kernel: one CTA per SM, never more CTAs than items.
-int attn_grid(int n_items, int num_sms);
+// Bytes of one partial record: unnormalised O of both tiles (fp32) plus the
+// row max and row sum of both tiles.
+inline size_t partial_record_bytes(int D) { return (size_t)2 * 128 * D * 4 + (size_t)2 * 2 * 128 * 4; }
+
+// Chooses the grid and fills the schedule fields of p. With a workspace the
+// tail waves are balanced; without one every CTA takes whole items only.
+int attn_schedule(AttnParams &p, int num_sms, bool balanced);
+// Workspace bytes a balanced call needs (records, then counters), 256-aligned parts.
+size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms);
 
 // epi = 0: head-partitioned output (same layout as q); epi = 1: All-to-All scatter.
 cudaError_t launch_attention(int D, int epi, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -49,6 +49,7 @@
 #ifndef XS_H
 #define XS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -63,7 +64,8 @@ typedef enum {
     XS_ERR_UNSUPPORTED = 4, /* D not in {64,128}, wrong GPU, or a pointer that is not device memory */
     XS_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed (message in xs_last_error) */
     XS_ERR_TIMEOUT = 6,     /* a bounded in-kernel wait ran out (reported by xs_device_status) */
-    XS_ERR_ALIAS = 7        /* out overlaps an input */
+    XS_ERR_ALIAS = 7,       /* out overlaps an input */
+    XS_ERR_WORKSPACE = 8    /* workspace too small, misaligned or overlapping */
 } xs_status;
 
 /*
@@ -98,6 +100,33 @@ xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B,
  * S % P == 0 (no multiple-of-128 rule). in and out must not overlap.
  */
 xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream);
+
+/*
+ * Balanced-schedule variants. Identical results contract and layouts as
+ * xs_attn_a2a / xs_attn, plus a caller-owned device workspace that lets the
+ * last one to two waves of work be split evenly over all SMs instead of
+ * leaving some SMs idle: an output tile pair whose K/V range is split across
+ * CTAs is computed in pieces whose partial rows (unnormalised O in fp32, row
+ * max, row sum) meet in the workspace and are merged in a fixed order.
+ *   workspace       : device memory, 256-byte aligned, at least the size that
+ *                     xs_attn_workspace_size reports for these shapes on the
+ *                     current device; its contents need no initialisation and
+ *                     may be left arbitrary between calls. NULL (with
+ *                     workspace_bytes = 0) falls back to the whole-item schedule.
+ *   workspace_bytes : its size in bytes.
+ * Calls that may run concurrently must not share a workspace. xs_attn_a2a_ws
+ * and xs_a2a_permute(xs_attn_ws(...)) are bit-identical for the same
+ * arguments on the same device; against the whole-item schedule the split
+ * tiles differ only by rounding.
+ */
+xs_status xs_attn_a2a_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                         int P, float scale, void *workspace, size_t workspace_bytes, void *stream);
+xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                     float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes that the *_ws calls need for these shapes on the current
+ * device (written to *bytes). Shape rules as for the attention calls. */
+xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *bytes);
 
 /* Human-readable description of the last non-OK status returned on this host
  * thread (empty string if none). The pointer stays valid until the next call

@@ -78,6 +78,22 @@ def test_attention_argument_checks(xs, fn_name):
     assert _attn(xs, fn, S=0) == xs.XS_OK
 
 
+def test_workspace_argument_checks(xs):
+    W = 0x50000000
+    f = lambda ws=W, nb=1 << 26, **kw: xs.attn_a2a_ws(Q, K, V, O, kw.get("B", 1), kw.get("S", 256), 8, 64, 4, 0.125,
+                                                      ws, nb, check=False)
+    assert f(ws=None, nb=64) == xs.XS_ERR_WORKSPACE        # NULL with a size
+    assert f(ws=W + 16) == xs.XS_ERR_WORKSPACE              # not 256-byte aligned
+    assert f(ws=O) == xs.XS_ERR_WORKSPACE                   # overlaps out
+    assert f(ws=V - 256, nb=4096) == xs.XS_ERR_WORKSPACE     # overlaps v
+    assert f(B=0) == xs.XS_OK                               # empty call
+    assert xs.attn_ws(0, K, V, O, 1, 256, 8, 64, 4, 0.1, W, 1 << 20, check=False) == xs.XS_ERR_NULL
+    n = ctypes.c_size_t(7)
+    assert xs.lib.xs_attn_workspace_size(1, 0, 8, 64, 4, ctypes.byref(n)) == xs.XS_OK and n.value == 0
+    assert xs.lib.xs_attn_workspace_size(1, 100, 8, 64, 4, ctypes.byref(n)) == xs.XS_ERR_SHAPE
+    assert xs.lib.xs_attn_workspace_size(1, 256, 8, 64, 4, None) == xs.XS_ERR_NULL
+
+
 def test_permute_argument_checks(xs):
     f = lambda i=Q, o=O, B=1, S=256, H=8, D=64, P=4: xs.a2a_permute(i, o, B, S, H, D, P, check=False)
     assert f(i=0) == xs.XS_ERR_NULL

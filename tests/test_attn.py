@@ -10,7 +10,8 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import (SENTINEL, assert_close, from_dev, run_paths, sample_rows, seq_rows_of, to_dev)
+from xs_testlib import (SENTINEL, assert_close, from_dev, run_paths, run_paths_ws, sample_rows, seq_rows_of,
+                        to_dev)
 
 # (B, S, H, D, P, sigma_qk, scale): small enough for a full oracle pass, yet
 # several tiles, lone last tiles, ranks whose token slice is not a multiple of
@@ -38,6 +39,60 @@ def test_small_parity(case):
     ref_head = oracle.attention(q, k, v, B, S, H, D, P, scale)
     assert_close(head, ref_head.ravel(), what="xs_attn")
     assert_close(fused, oracle.a2a(ref_head, B, S, H, D, P).ravel(), what="xs_attn_a2a")
+
+
+# Shapes for the balanced schedule: items that are not a multiple of the grid
+# (tail waves split into pieces), and far fewer items than SMs (one item cut
+# into many pieces across many CTAs).
+BALANCED = [
+    (1, 4096, 4, 128, 2, 1.0, 128 ** -0.5),    # 64 items of 32 K/V tiles over 152 CTAs: ~3 pieces each
+    (1, 2048, 40, 64, 4, 1.0, 1 / 8),           # 320 items: two whole waves + balanced tail
+    (2, 1152, 38, 128, 2, 1.0, 128 ** -0.5),    # 380 items, lone last tiles, B = 2
+    (1, 384, 2, 128, 1, 2.0, 0.35),             # 4 items over 12 units, peaked
+    (1, 256, 8, 64, 4, 1.0, 1 / 8),             # the small workload
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", SMALL[:3] + BALANCED)
+def test_balanced_parity(case):
+    B, S, H, D, P, sigma, scale = case
+    q, k, v = xsgen.random_inputs(300 + S + H + D, P, B, S, H, D, sigma, 1.0)
+    fused, head, serial = run_paths_ws(q, k, v, B, S, H, D, P, scale, fill=0xA5)
+    assert not (fused == SENTINEL).any() and not (head == SENTINEL).any()
+    assert np.array_equal(fused, serial), "balanced fused != balanced attn then permute"
+    if B * S * H * D <= 40 * 2048 * 64:
+        ref_head = oracle.attention(q, k, v, B, S, H, D, P, scale)
+        assert_close(head, ref_head.ravel(), what="xs_attn_ws")
+        assert_close(fused, oracle.a2a(ref_head, B, S, H, D, P).ravel(), what="xs_attn_a2a_ws")
+    else:
+        rows = sample_rows(B, S, H, P, 2000, 5)
+        ref = oracle.attention_rows(q, k, v, B, S, H, D, P, scale, rows)
+        assert_close(fused.reshape(-1, D)[seq_rows_of(rows, B, S, H, D, P)], ref, what="xs_attn_a2a_ws rows")
+
+
+@pytest.mark.gpu
+def test_balanced_reuses_dirty_workspace():
+    """Back-to-back calls on one workspace (stale counters and records from the
+    previous call) give identical results."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    B, S, H, D, P = 1, 4096, 4, 128, 2
+    q, k, v = xsgen.random_inputs(41, P, B, S, H, D)
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    nb = xs.workspace_size(B, S, H, D, P)
+    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        o = torch.empty(B * S * H * D, dtype=torch.int16, device="cuda")
+        xs.attn_a2a_ws(tq, tk, tv, o, B, S, H, D, P, 0.1, ws)
+        outs.append(from_dev(o))
+    torch.cuda.synchronize()
+    assert xs.device_status() == xs.XS_OK
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    o = torch.empty(B * S * H * D, dtype=torch.int16, device="cuda")
+    assert xs.attn_a2a_ws(tq, tk, tv, o, B, S, H, D, P, 0.1, small, check=False) == xs.XS_ERR_WORKSPACE
 
 
 @pytest.mark.gpu
@@ -72,12 +127,14 @@ def test_workload_full_size(idx):
     w = xsgen.WORKLOADS[idx]
     B, S, H, D, P = w["B"], w["S"], w["H"], w["D"], w["P"]
     q, k, v = xsgen.workload_inputs(idx)
-    fused, head, serial = run_paths(q, k, v, B, S, H, D, P, w["scale"])
-    assert not (fused == SENTINEL).any()
-    assert np.array_equal(fused, serial), "fused != attn then permute"
     rows = sample_rows(B, S, H, P, 1024, idx)
     ref = oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], rows)
-    assert_close(fused.reshape(-1, D)[seq_rows_of(rows, B, S, H, D, P)], ref, what=w["name"])
+    seq_rows = seq_rows_of(rows, B, S, H, D, P)
+    for runner in (run_paths, run_paths_ws):
+        fused, head, serial = runner(q, k, v, B, S, H, D, P, w["scale"])
+        assert not (fused == SENTINEL).any()
+        assert np.array_equal(fused, serial), f"{runner.__name__}: fused != attn then permute"
+        assert_close(fused.reshape(-1, D)[seq_rows], ref, what=f"{w['name']} {runner.__name__}")
 
 
 @pytest.mark.gpu

@@ -76,3 +76,25 @@ def seq_rows_of(head_rows, B, S, H, D, P):
         r, b = rb // B, rb % B
         out.append(oracle.seq_offset(b, s, r * Hl + hl, 0, B, S, H, D, P) // D)
     return np.array(out, dtype=np.int64)
+
+
+def run_paths_ws(q, k, v, B, S, H, D, P, scale, fill=None, stream=None):
+    """Balanced-schedule paths: (fused_ws, head_ws, serial_ws) as uint16 arrays. The
+    workspace is allocated here and, if `fill` is given, pre-filled with that byte."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    n = P * B * S * (H // P) * D
+    nb = xs.workspace_size(B, S, H, D, P)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    if fill is not None:
+        ws.fill_(fill)
+    fused = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    head = torch.full_like(fused, -1)
+    serial = torch.full_like(fused, -1)
+    xs.attn_a2a_ws(tq, tk, tv, fused, B, S, H, D, P, scale, ws, nb, stream=stream)
+    xs.attn_ws(tq, tk, tv, head, B, S, H, D, P, scale, ws, nb, stream=stream)
+    xs.a2a_permute(head, serial, B, S, H, D, P, stream=stream)
+    torch.cuda.synchronize()
+    assert xs.device_status() == xs.XS_OK, xs.last_error()
+    return from_dev(fused), from_dev(head), from_dev(serial)
