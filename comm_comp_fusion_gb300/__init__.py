@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIG
 
 # Every symbol include/xs.h declares.
 EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size",
-           "xs_last_error", "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
+           "xs_attn_a2a_noalloc", "xs_last_error", "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
 
 
 class XsError(RuntimeError):
@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
     lib.xs_attn_ws.restype = i
     lib.xs_attn_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
     lib.xs_attn_workspace_size.restype = i
+    lib.xs_attn_a2a_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.xs_attn_a2a_noalloc.restype = i
     lib.xs_last_error.argtypes = []
     lib.xs_last_error.restype = ctypes.c_char_p
     lib.xs_device_status.argtypes = [vp, i]
@@ -143,6 +145,14 @@ def workspace_size(B, S, H, D, P) -> int:
     n = ctypes.c_size_t(0)
     _check(lib.xs_attn_workspace_size(B, S, H, D, P, ctypes.byref(n)))
     return n.value
+
+
+def attn_a2a_noalloc(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
+    """Balanced fused call on the library's built-in scratch (``xs_attn_a2a_noalloc``),
+    for callers that cannot allocate a workspace; returns the status."""
+    st = lib.xs_attn_a2a_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale),
+                                 _stream(stream, q, out))
+    return _check(st) if check else st
 
 
 def a2a_permute(inp, out, B, S, H, D, P, stream=None, check=True):

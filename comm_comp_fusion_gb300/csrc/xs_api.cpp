@@ -209,6 +209,12 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
 
 }  // namespace
 
+namespace xs {
+// Records `message` as this thread's last error and returns `status`; for the
+// other translation units of the library.
+int report_error(int status, const char *message) { return (int)fail((xs_status)status, "%s", message); }
+}  // namespace xs
+
 extern "C" {
 
 xs_status xs_attn_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,

@@ -49,6 +49,9 @@ size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms);
 cudaError_t launch_attention(int D, int epi, const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const AttnParams &p, int grid, cudaStream_t stream);
 
+// Sets the calling thread's xs_last_error() text; returns `status`.
+int report_error(int status, const char *message);
+
 // Device-side error word (bit 31: a bounded wait ran out; low bits: which wait).
 cudaError_t read_device_error(unsigned int *value, bool clear, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);

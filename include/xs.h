@@ -128,6 +128,30 @@ xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int
  * device (written to *bytes). Shape rules as for the attention calls. */
 xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *bytes);
 
+/*
+ * The balanced fused call for callers that cannot allocate device memory. The
+ * paper has no counterpart to this call; it exists for deployment.
+ * Some callers can pass q, k, v and out but cannot allocate a workspace: a
+ * plug-in inside a framework that owns all device memory through its own pool,
+ * a latency-critical path that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation, or a process whose device memory is reserved up front.
+ * This call computes what xs_attn_a2a_ws computes (same arguments minus the
+ * workspace), using instead a scratch area built into the library: 48 MiB per
+ * device that loads the library, held until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Shapes whose balanced schedule needs more than the 48 MiB are rejected
+ *     with XS_ERR_WORKSPACE before anything is enqueued
+ *     (xs_attn_workspace_size reports the need).
+ *   - Every call on a device shares the one scratch area, which keeps the
+ *     previous call's contents; its counters are cleared on the calling stream
+ *     before each launch. Calls that may overlap on the GPU race on the scratch
+ *     area and must not be issued.
+ *   - The first call on a device looks up the scratch area's device address
+ *     with that device current; make that first call before any stream capture.
+ */
+xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void *out, int B, int S, int H,
+                              int D, int P, float scale, void *stream);
+
 /* Human-readable description of the last non-OK status returned on this host
  * thread (empty string if none). The pointer stays valid until the next call
  * on this thread. */
