@@ -82,6 +82,7 @@ __device__ __forceinline__ bool warp_bwait(uint32_t bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+
 template <int D> struct Cfg {
     static constexpr int kNDB = D / 64;                 // 64-column (128-byte) swizzle blocks per row
     static constexpr uint32_t kBlk = 128u * 128u;       // one swizzle block of a 128-row tile
@@ -332,11 +333,12 @@ __global__ void __launch_bounds__(512, 1)
                     tc_mma_ss(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_PV = [&](int t, uint32_t slot, bool acc) {
+            // O_t (+)= P_t V for K/V rows [16*k0, 16*k1) of the tile
+            auto issue_PV = [&](int t, uint32_t slot, bool acc, int k0, int k1) {
                 const uint64_t va = dV + (opaque(sKV + slot * C::kTile) >> 4);
                 const uint32_t d = opaque(tmem + C::colO(t)), a = opaque(tmem + C::colS(t));
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
+                for (int kk = k0; kk < k1; ++kk)
                     tc_mma_ts(d, a + kk * 8, va + (kk * 2048 >> 4), idO, (acc || kk > 0) ? 1u : 0u);
             };
             uint32_t kv_it = 0, it = 0, pph0 = 0, pph1 = 0;
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (!ok) break;
                     pph0 ^= 1u;
                     tc_fence_after();
-                    issue_PV(0, vslot, j > 0);
+                    issue_PV(0, vslot, j > 0, 0, 8);
                     if (!more) tc_commit(BAR(BO_FINAL + 0));
                     if (more) {
                         kslot = kv_it % C::kSlots;
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (!ok) break;
                     pph1 ^= 1u;
                     tc_fence_after();
-                    issue_PV(1, vslot, j > 0);
+                    issue_PV(1, vslot, j > 0, 0, 8);
                     tc_commit(BAR(BKV_EMPTY + vslot));
                     if (!more) tc_commit(BAR(BO_FINAL + 1));
                     if (more) {
@@ -433,19 +435,29 @@ __global__ void __launch_bounds__(512, 1)
                 if (!ok) break;
                 sph ^= 1u;
                 tc_fence_after();
-                uint32_t s[128];
-                tmem_ld128(tS, s);
-                // row max: four chains of three-input max
-                float mx0 = fmaxf(u2f(s[0]), u2f(s[1])), mx1 = fmaxf(u2f(s[2]), u2f(s[3]));
-                float mx2 = fmaxf(u2f(s[4]), u2f(s[5])), mx3 = fmaxf(u2f(s[6]), u2f(s[7]));
+                // this thread's row of S: columns 0-63 in sa, 64-127 in sb
+                uint32_t sa[64], sb[64];
+#define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
+                tmem_ld64(tS, sa);
+                tmem_ld64(tS + 64, sb);
+                float mx0 = fmaxf(u2f(sa[0]), u2f(sa[1])), mx1 = fmaxf(u2f(sa[2]), u2f(sa[3]));
+                float mx2 = fmaxf(u2f(sa[4]), u2f(sa[5])), mx3 = fmaxf(u2f(sa[6]), u2f(sa[7]));
 #pragma unroll
-                for (int i = 8; i < 128; i += 8) {
-                    mx0 = fmax3(mx0, u2f(s[i + 0]), u2f(s[i + 1]));
-                    mx1 = fmax3(mx1, u2f(s[i + 2]), u2f(s[i + 3]));
-                    mx2 = fmax3(mx2, u2f(s[i + 4]), u2f(s[i + 5]));
-                    mx3 = fmax3(mx3, u2f(s[i + 6]), u2f(s[i + 7]));
+                for (int i = 8; i < 64; i += 8) {
+                    mx0 = fmax3(mx0, u2f(sa[i + 0]), u2f(sa[i + 1]));
+                    mx1 = fmax3(mx1, u2f(sa[i + 2]), u2f(sa[i + 3]));
+                    mx2 = fmax3(mx2, u2f(sa[i + 4]), u2f(sa[i + 5]));
+                    mx3 = fmax3(mx3, u2f(sa[i + 6]), u2f(sa[i + 7]));
                 }
-                const float mnew = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+#pragma unroll
+                for (int i = 0; i < 64; i += 8) {
+                    mx0 = fmax3(mx0, u2f(sb[i + 0]), u2f(sb[i + 1]));
+                    mx1 = fmax3(mx1, u2f(sb[i + 2]), u2f(sb[i + 3]));
+                    mx2 = fmax3(mx2, u2f(sb[i + 4]), u2f(sb[i + 5]));
+                    mx3 = fmax3(mx3, u2f(sb[i + 6]), u2f(sb[i + 7]));
+                }
+                const float rowmax = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+                const float mnew = rowmax * sl2;
                 float alpha = 1.f;
                 bool need = false;
                 if (j == 0) {
@@ -471,29 +483,32 @@ __global__ void __launch_bounds__(512, 1)
                 // p = exp2(s * scale*log2e - m): paired FMAs, ex2, paired sums, bf16 pairs
                 const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
                 uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-                uint32_t pa[32], pb[32];
 #pragma unroll
-                for (int i = 0; i < 64; i += 2) {
-                    float e0, e1, e2, e3;
-                    f2unpack(ffma2(f2pack(u2f(s[2 * i]), u2f(s[2 * i + 1])), sc2, nm2), e0, e1);
-                    f2unpack(ffma2(f2pack(u2f(s[2 * i + 2]), u2f(s[2 * i + 3])), sc2, nm2), e2, e3);
-                    e0 = ex2_approx(e0);
-                    e1 = ex2_approx(e1);
-                    e2 = ex2_approx(e2);
-                    e3 = ex2_approx(e3);
-                    acc0 = fadd2(acc0, f2pack(e0, e1));
-                    acc1 = fadd2(acc1, f2pack(e2, e3));
-                    uint32_t *dstp = i < 32 ? &pa[i & 31] : &pb[i & 31];
-                    dstp[0] = pack_bf16x2(e0, e1);
-                    dstp[1] = pack_bf16x2(e2, e3);
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int e = 64 * hf + 2 * i;
+                        float e0, e1, e2, e3;
+                        f2unpack(ffma2(f2pack(SV(e), SV(e + 1)), sc2, nm2), e0, e1);
+                        f2unpack(ffma2(f2pack(SV(e + 2), SV(e + 3)), sc2, nm2), e2, e3);
+                        e0 = ex2_approx(e0);
+                        e1 = ex2_approx(e1);
+                        e2 = ex2_approx(e2);
+                        e3 = ex2_approx(e3);
+                        acc0 = fadd2(acc0, f2pack(e0, e1));
+                        acc1 = fadd2(acc1, f2pack(e2, e3));
+                        pk[i] = pack_bf16x2(e0, e1);
+                        pk[i + 1] = pack_bf16x2(e2, e3);
+                    }
+                    tmem_st32(tS + 32 * hf, pk);
                 }
+#undef SV
                 {
                     float a0, a1;
                     f2unpack(fadd2(acc0, acc1), a0, a1);
                     l += a0 + a1;
                 }
-                tmem_st32(tS, pa);
-                tmem_st32(tS + 32, pb);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
