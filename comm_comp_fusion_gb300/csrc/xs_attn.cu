@@ -51,7 +51,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s; a whole call
 
 enum WaitSite : uint32_t {
     kSiteLoadQ = 0, kSiteLoadKV, kSiteMmaQ, kSiteMmaKV, kSiteMmaP, kSiteMmaOFree, kSiteSoftS,
-    kSiteSoftL, kSiteEpiO, kSiteEpiL, kSiteDrain, kSiteSelftest
+    kSiteSoftL, kSiteEpiO, kSiteEpiL, kSiteDrain, kSiteSelftest, kSiteSoftO
 };
 
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
@@ -180,6 +180,13 @@ __device__ __forceinline__ bool sched_next(Sched &s, const AttnParams &p, Seg &g
     return true;
 }
 
+// True when the segment just returned by sched_next is this CTA's last.
+__device__ __forceinline__ bool sched_done(const Sched &s, const AttnParams &p) {
+    Sched t = s;
+    Seg g;
+    return !sched_next(t, p, g);
+}
+
 // Counts an arrival on a counter stamped with this call's generation (low 12
 // bits: arrivals, high 20: generation; a stale stamp counts as zero). Returns
 // true for the n-th arrival. The CAS loop ends after at most n retries.
@@ -223,6 +230,180 @@ __device__ __forceinline__ uint32_t opaque(uint32_t x) {
     return x;
 }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+// ----------------------------------------------------------------- output rows
+// Output rows go through shared memory: each lane writes 16-byte chunk c (8
+// bf16) of its own row into staging row `lane` (XOR-swizzled), then the warp
+// copies its 32 rows out with coalesced 16-byte stores, 128 bytes per row.
+__device__ __forceinline__ void stage_chunk(uint32_t stage, int lane, int c, uint32_t x0, uint32_t x1, uint32_t x2,
+                                            uint32_t x3) {
+    const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1), "r"(x2), "r"(x3) : "memory");
+}
+__device__ __forceinline__ void flush_block(uint16_t *out, uint32_t stage, int lane, int64_t dst, int db) {
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = i * 32 + lane;
+        const int rr = idx >> 3, c = idx & 7;
+        const uint32_t a = stage + rr * 128 + ((c ^ (rr & 7)) << 4);
+        uint32_t y0, y1, y2, y3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3) : "r"(a) : "memory");
+        const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
+        uint16_t *gp = out + d + db * 64 + c * 8;
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gp), "r"(y0), "r"(y1), "r"(y2), "r"(y3) : "memory");
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------ split items
+// Floats in one partial record: unnormalised O of both tiles as
+// [tile][D/4][128 rows][4], then [tile][row max, row sum][128].
+template <int D> struct Rec {
+    static constexpr size_t kFloats = 2 * 128 * D + 2 * 2 * 128;
+    static constexpr size_t kML = 2 * 128 * D;
+};
+
+// Record of the piece of the split item starting at unit ua that CTA c computed.
+__device__ __forceinline__ const float *piece_record(const AttnParams &p, int c, uint32_t ua, size_t rec_floats) {
+    const int slot = 2 * c + (sk_start((uint32_t)c, p) >= ua ? 0 : 1);
+    return p.ws_rec + (size_t)slot * rec_floats;
+}
+
+// Merge of a split item's pieces for one warp's 32 rows of tile t, in piece
+// order, and the store of the final rows. With self_tmem the piece computed by
+// this CTA is read from tensor memory (it never went to the workspace);
+// otherwise every piece, this CTA's included, comes from the workspace. Both
+// read the same bits, so the result does not depend on which piece merges.
+// CH columns (32 or 64) are gathered per round.
+template <int D, int CH>
+__device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, int lane, uint32_t stage, int c_first,
+                                           int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
+                                           uint32_t tO, int64_t dst, bool valid) {
+    using R = Rec<D>;
+    const int self = (int)blockIdx.x;
+    float M = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c)
+        M = fmaxf(M, (self_tmem && c == self) ? m_self
+                                             : ld_cg(piece_record(p, c, ua, R::kFloats) + R::kML + t * 256 + row));
+    float L = 0.f;
+    for (int c = c_first; c <= c_last; ++c) {
+        float mc, lc;
+        if (self_tmem && c == self) {
+            mc = m_self;
+            lc = l_self;
+        } else {
+            const float *r = piece_record(p, c, ua, R::kFloats) + R::kML + t * 256;
+            mc = ld_cg(r + row);
+            lc = ld_cg(r + 128 + row);
+        }
+        L += ex2_approx(mc - M) * lc;
+    }
+    const float inv_L = 1.0f / L;
+#pragma unroll 1
+    for (int col0 = 0; col0 < D; col0 += CH) {
+        float acc[CH];
+#pragma unroll
+        for (int i = 0; i < CH; ++i) acc[i] = 0.f;
+        for (int c = c_first; c <= c_last; ++c) {
+            if (self_tmem && c == self) {
+                const float wk = ex2_approx(m_self - M);
+#pragma unroll
+                for (int h = 0; h < CH; h += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + col0 + h, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[h + i] = fmaf(wk, __uint_as_float(o[i]), acc[h + i]);
+                }
+            } else {
+                const float *r = piece_record(p, c, ua, R::kFloats);
+                const float wk = ex2_approx(ld_cg(r + R::kML + t * 256 + row) - M);
+                const float4 *src = reinterpret_cast<const float4 *>(r) + (size_t)t * (D / 4) * 128;
+                float4 v[CH / 4];
+#pragma unroll
+                for (int q = 0; q < CH / 4; ++q) v[q] = ld_cg4(src + (size_t)(col0 / 4 + q) * 128 + row);
+#pragma unroll
+                for (int q = 0; q < CH / 4; ++q) {
+                    acc[4 * q] = fmaf(wk, v[q].x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(wk, v[q].y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wk, v[q].z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wk, v[q].w, acc[4 * q + 3]);
+                }
+            }
+        }
+        if (valid) {
+#pragma unroll
+            for (int c = 0; c < CH / 8; ++c)
+                stage_chunk(stage, lane, (col0 % 64) / 8 + c, pack_bf16x2(acc[8 * c + 0] * inv_L, acc[8 * c + 1] * inv_L),
+                            pack_bf16x2(acc[8 * c + 2] * inv_L, acc[8 * c + 3] * inv_L),
+                            pack_bf16x2(acc[8 * c + 4] * inv_L, acc[8 * c + 5] * inv_L),
+                            pack_bf16x2(acc[8 * c + 6] * inv_L, acc[8 * c + 7] * inv_L));
+            if ((col0 + CH) % 64 == 0) flush_block(p.out, stage, lane, dst, col0 / 64);
+        }
+    }
+}
+
+// One warp's 32 rows of tile t of a split piece, after its last PV: either
+// merge now (every other piece already arrived; this piece is read from
+// TMEM) and return 0, or publish this piece's rows (unnormalised O, row max,
+// row sum) to the workspace and return 1: the caller must then count the
+// arrival with arrive_piece. `release` runs once the rows are out of TMEM.
+template <int D, int CH, typename Release>
+__device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
+                                                 uint32_t stage, int c_first, int c_last, uint32_t ua, float m, float l,
+                                                 uint32_t tO, int64_t dst, bool valid, Release release) {
+    using R = Rec<D>;
+    const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
+    const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
+    uint32_t *cnt = p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq);
+    uint32_t others = 0;
+    if (lane == 0) {
+        const uint32_t v = *reinterpret_cast<volatile uint32_t *>(cnt);
+        others = ((v >> 12) == (p.gen & 0xFFFFFu) && (v & 0xFFFu) == npieces - 1u) ? 1u : 0u;
+    }
+    others = __shfl_sync(0xffffffffu, others, 0);
+    if (others) {
+        __threadfence();
+        merge_rows<D, CH>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst, valid);
+        release();
+        return 0;
+    }
+    const int own_slot = 2 * (int)blockIdx.x + (g.first ? 0 : 1);
+    float *rec = p.ws_rec + (size_t)own_slot * R::kFloats;
+    float4 *o4 = reinterpret_cast<float4 *>(rec) + (size_t)t * (D / 4) * 128;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c, o);
+        if (c + 32 == D) release();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            o4[(size_t)(c / 4 + q) * 128 + row] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                                              __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+    }
+    rec[R::kML + t * 256 + row] = m;
+    rec[R::kML + t * 256 + 128 + row] = l;
+    return 1;
+}
+
+// Counts this piece's arrival for tile t (after its rows were published and
+// fenced); the last arrival merges from the workspace.
+template <int D, int CH>
+__device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
+                                             uint32_t stage, int c_first, int c_last, uint32_t ua, int64_t dst,
+                                             bool valid) {
+    const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
+    uint32_t last = 0;
+    if (lane == 0)
+        last = arrive_last(p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq), p.gen, (uint32_t)(c_last - c_first + 1))
+                   ? 1u
+                   : 0u;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    merge_rows<D, CH>(p, t, row, lane, stage, c_first, c_last, ua, false, 0.f, 0.f, 0u, dst, valid);
+}
+
 
 template <int D, int EPI>
 __global__ void __launch_bounds__(512, 1)
@@ -515,6 +696,30 @@ __global__ void __launch_bounds__(512, 1)
                 if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
             }
             if (!ok) break;
+            if (g.split && sched_done(sch, p)) {
+                // This CTA's last piece of a split item: finish tile t here, both
+                // tiles in parallel, instead of handing it to the epilogue. Every
+                // MMA of the CTA is complete once O_t is final, so the query
+                // tile's shared memory is free and serves as staging.
+                ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteSoftO);
+                if (!ok) break;
+                tc_fence_after();
+                const Item w = decode_item(p, g.item);
+                const uint32_t ua = (uint32_t)(g.item - p.sk_item0) * (uint32_t)p.n_kv;
+                const int c_first = sk_cta_of(ua, p), c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
+                const int qt = 2 * w.pair + t;
+                const bool valid = qt < p.n_qt;
+                const int64_t dst = out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row);
+                const uint32_t stage = sQ + t * C::kTile + (warp & 3) * C::kStageWarp;
+                const uint32_t pend = finish_piece<D, 64>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
+                                                          l, tO, dst, valid, [] {});
+                if (pend) {
+                    __threadfence();
+                    __syncwarp();
+                    arrive_piece<D, 64>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst, valid);
+                }
+                continue;
+            }
             ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
             if (!ok) break;
             row_ml[t * 256 + row] = l;
@@ -529,123 +734,22 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const int row = wq * 32 + lane;
         const uint32_t stage = sStage + wq * C::kStageWarp;
-        constexpr size_t kRecFloats = 2 * 128 * D + 2 * 2 * 128;
-        // Output rows go through shared memory: each lane writes 16-byte chunk c
-        // (8 bf16) of its own row into staging row `lane` (XOR-swizzled), then
-        // the warp copies its 32 rows out with coalesced 16-byte stores.
-        auto stage_chunk = [&](int c, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
-            const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1), "r"(x2), "r"(x3)
-                         : "memory");
-        };
-        auto flush_block = [&](int64_t dst, int db) {
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int idx = i * 32 + lane;
-                const int rr = idx >> 3, c = idx & 7;
-                const uint32_t a = stage + rr * 128 + ((c ^ (rr & 7)) << 4);
-                uint32_t y0, y1, y2, y3;
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3)
-                             : "r"(a)
-                             : "memory");
-                const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
-                uint16_t *gp = p.out + d + db * 64 + c * 8;
-                asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gp), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-                             : "memory");
-            }
-            __syncwarp();
-        };
-        // Merge of a split item's pieces for this warp's 32 rows of tile t, in
-        // piece order. With self_tmem the piece computed by this CTA is read from
-        // tensor memory (it never went to the workspace); otherwise every piece,
-        // this CTA's included, comes from the workspace. Both read the same bits,
-        // so the result does not depend on which piece merges.
-        auto merge = [&](int t, int c_first, int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
-                         uint32_t tO, int64_t dst, bool valid) {
-            auto piece = [&](int c) -> const float * {
-                const int slot = 2 * c + (sk_start((uint32_t)c, p) >= ua ? 0 : 1);
-                return p.ws_rec + (size_t)slot * kRecFloats;
-            };
-            const int self = (int)blockIdx.x;
-            float M = -INFINITY;
-            for (int c = c_first; c <= c_last; ++c)
-                M = fmaxf(M, (self_tmem && c == self) ? m_self : ld_cg(piece(c) + 2 * 128 * D + t * 256 + row));
-            float L = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {
-                float mc, lc;
-                if (self_tmem && c == self) {
-                    mc = m_self;
-                    lc = l_self;
-                } else {
-                    const float *r = piece(c) + 2 * 128 * D + t * 256;
-                    mc = ld_cg(r + row);
-                    lc = ld_cg(r + 128 + row);
-                }
-                L += ex2_approx(mc - M) * lc;
-            }
-            const float inv_L = 1.0f / L;
-#pragma unroll 1
-            for (int db = 0; db < C::kNDB; ++db) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int col = db * 64 + h * 32;
-                    float acc[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                    for (int c = c_first; c <= c_last; ++c) {
-                        if (self_tmem && c == self) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + col, o);
-                            const float wk = ex2_approx(m_self - M);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) acc[i] = fmaf(wk, u2f(o[i]), acc[i]);
-                        } else {
-                            const float *r = piece(c);
-                            const float wk = ex2_approx(ld_cg(r + 2 * 128 * D + t * 256 + row) - M);
-                            const float4 *src = reinterpret_cast<const float4 *>(r) + (size_t)t * (D / 4) * 128;
-                            float4 v[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) v[q] = ld_cg4(src + (size_t)(col / 4 + q) * 128 + row);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                acc[4 * q] = fmaf(wk, v[q].x, acc[4 * q]);
-                                acc[4 * q + 1] = fmaf(wk, v[q].y, acc[4 * q + 1]);
-                                acc[4 * q + 2] = fmaf(wk, v[q].z, acc[4 * q + 2]);
-                                acc[4 * q + 3] = fmaf(wk, v[q].w, acc[4 * q + 3]);
-                            }
-                        }
-                    }
-                    if (valid) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            stage_chunk(4 * h + c, pack_bf16x2(acc[8 * c + 0] * inv_L, acc[8 * c + 1] * inv_L),
-                                        pack_bf16x2(acc[8 * c + 2] * inv_L, acc[8 * c + 3] * inv_L),
-                                        pack_bf16x2(acc[8 * c + 4] * inv_L, acc[8 * c + 5] * inv_L),
-                                        pack_bf16x2(acc[8 * c + 6] * inv_L, acc[8 * c + 7] * inv_L));
-                    }
-                }
-                if (valid) flush_block(dst, db);
-            }
-        };
         uint32_t it = 0;
         bool ok = true;
         Sched sch;
         sched_init(sch, p);
         Seg g;
         for (; ok && sched_next(sch, p, g); ++it) {
+            // a CTA's last piece of a split item is finished by the softmax warpgroups
+            if (g.split && sched_done(sch, p)) continue;
             const Item w = decode_item(p, g.item);
-            // a split item: which CTAs hold its pieces, and this CTA's record
-            const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
-            const uint32_t ua = x_local * (uint32_t)p.n_kv;  // the item's first unit
+            const uint32_t ua = (uint32_t)(g.item - p.sk_item0) * (uint32_t)p.n_kv;  // a split item's first unit
             int c_first = 0, c_last = 0;
             if (g.split) {
                 c_first = sk_cta_of(ua, p);
                 c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
             }
-            const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
-            uint32_t pending = 0;  // tiles whose partial went to the workspace
+            uint32_t pending = 0;  // tiles whose rows went to the workspace
             for (int t = 0; t < 2; ++t) {
                 ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteEpiO) &&
                      warp_bwait(BAR(BL_FULL + t), it & 1u, abort_flag, kSiteEpiL);
@@ -664,72 +768,37 @@ __global__ void __launch_bounds__(512, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
                 };
-                if (!g.split) {
-                    const float inv_l = 1.0f / l;
-#pragma unroll 1
-                    for (int db = 0; db < C::kNDB; ++db) {
-                        uint32_t o[64];
-                        tmem_ld64(tO + db * 64, o);
-                        if (db == C::kNDB - 1) release_o();
-                        if (!valid) continue;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            stage_chunk(c, pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
-                        flush_block(dst, db);
-                    }
+                if (g.split) {
+                    pending |= finish_piece<D, 32>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO, dst,
+                                                   valid, release_o)
+                               << t;
                     continue;
                 }
-                // ---- a piece of a split item. If every other piece has already
-                // arrived, merge now, reading this piece straight from TMEM.
-                uint32_t *cnt = p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq);
-                uint32_t others = 0;
-                if (lane == 0) {
-                    const uint32_t v = *reinterpret_cast<volatile uint32_t *>(cnt);
-                    others = ((v >> 12) == (p.gen & 0xFFFFFu) && (v & 0xFFFu) == npieces - 1u) ? 1u : 0u;
-                }
-                others = __shfl_sync(0xffffffffu, others, 0);
-                if (others) {
-                    __threadfence();
-                    merge(t, c_first, c_last, ua, true, m, l, tO, dst, valid);
-                    release_o();
-                    continue;
-                }
-                // otherwise publish this piece's rows: unnormalised O, row max, row sum
-                const int own_slot = 2 * (int)blockIdx.x + (g.first ? 0 : 1);
-                float *rec = p.ws_rec + (size_t)own_slot * kRecFloats;
-                float4 *o4 = reinterpret_cast<float4 *>(rec) + (size_t)t * (D / 4) * 128;
+                const float inv_l = 1.0f / l;
 #pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c, o);
-                    if (c + 32 == D) release_o();
+                for (int db = 0; db < C::kNDB; ++db) {
+                    uint32_t o[64];
+                    tmem_ld64(tO + db * 64, o);
+                    if (db == C::kNDB - 1) release_o();
+                    if (!valid) continue;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        o4[(size_t)(c / 4 + q) * 128 + row] =
-                            make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]), u2f(o[4 * q + 3]));
+                    for (int c = 0; c < 8; ++c)
+                        stage_chunk(stage, lane, c, pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
+                                    pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
+                                    pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
+                                    pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
+                    flush_block(p.out, stage, lane, dst, db);
                 }
-                rec[2 * 128 * D + t * 256 + row] = m;
-                rec[2 * 128 * D + t * 256 + 128 + row] = l;
-                pending |= 1u << t;
             }
             if (!ok || !pending) continue;
-            // ---- count this piece's arrival for the published tiles; the last arrival merges
+            // count this piece's arrival for the published tiles; the last arrival merges
             __threadfence();
             __syncwarp();
             for (int t = 0; t < 2; ++t) {
                 if (!(pending & (1u << t))) continue;
-                uint32_t last = 0;
-                if (lane == 0)
-                    last = arrive_last(p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq), p.gen, npieces) ? 1u : 0u;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (!last) continue;
-                __threadfence();
                 const int qt = 2 * w.pair + t;
-                merge(t, c_first, c_last, ua, false, 0.f, 0.f, 0u,
-                      out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
+                arrive_piece<D, 32>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
+                                    out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
             }
         }
     }
