@@ -16,7 +16,11 @@ The line also reports, from a second timed region in the same run, the
 attention-only time, the serial composition (attention, then the standalone
 permute) and the permute alone, from which the overhead of the fused scatter
 over attention alone (E_res), the hiding ratio H and the speedup over serial
-follow (X-Stage paper, arXiv 2607.23264v1, section 5.3, Eq. 21). ``e2e``
+follow (X-Stage paper, arXiv 2607.23264v1, section 5.3, Eq. 21). A third
+region times ``xs_ulysses_attn`` (both Ulysses All-to-Alls fused: Q, K, V read
+from and O written to the sequence partition) against the post-only fused call
+and against its serial composition (three pre-attention permutes, attention,
+the post-attention permute); it is reported under ``ulysses``. ``e2e``
 times the same call with the inputs copied in from pinned host memory and the
 output copied back inside the timed region.
 
@@ -277,6 +281,22 @@ def run_ours(args):
         attn()
         perm()
 
+    # Both Ulysses All-to-Alls (section 4.3, Figure 5): the same q, k, v buffers
+    # read as sequence-partitioned [P][B][Sl][H][D] (same size, same i.i.d.
+    # values), against the serial composition: the pre-attention permute of each
+    # operand, attention, and the post-attention permute.
+    hq, hk, hv = (torch.empty_like(out) for _ in range(3))
+    uly_out = torch.empty_like(out)
+    ulysses = lambda: xs.ulysses_attn(q, k, v, uly_out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+    inv_perm = lambda: xs.a2a_permute_inverse(q, hq, B, S, H, D, P, stream=sptr)
+
+    def ulysses_serial():
+        inv_perm()
+        xs.a2a_permute_inverse(k, hk, B, S, H, D, P, stream=sptr)
+        xs.a2a_permute_inverse(v, hv, B, S, H, D, P, stream=sptr)
+        xs.attn_ws(hq, hk, hv, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+        perm()
+
     def timed(fns, steps):
         """Per-launch CUDA-event times (ms) of each fn, L2 flushed before each, order rotated."""
         ev = {i: [] for i in range(len(fns))}
@@ -299,6 +319,8 @@ def run_ours(args):
         fused_whole()
         attn()
         perm()
+        ulysses()
+        ulysses_serial()
     torch.cuda.synchronize(dev)
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
 
@@ -321,6 +343,10 @@ def run_ours(args):
     # every variant alike: fused, attention only, serial (attention + permute),
     # permute only, and the whole-item fused call
     t_fused_cmp, t_attn, t_serial, t_perm, t_whole = timed([fused, attn, serial_fn, perm, fused_whole], args.steps)
+    # ---- Ulysses region: both All-to-Alls fused vs the post-only fused call
+    # (the difference is the cost of reading from the sequence partition) and
+    # vs the serial composition
+    t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps)
     clocks = sampler.stop()
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
 
@@ -359,6 +385,7 @@ def run_ours(args):
     hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
     traffic = recorded_traffic(w["name"])
+    tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -386,6 +413,14 @@ def run_ours(args):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic,
                      "algorithmic_flop_per_launch": flops, "algorithmic_min_bytes_per_launch": 4 * nbytes},
+        "ulysses": {
+            "call": "xs_ulysses_attn (q, k, v, out sequence-partitioned; balanced schedule)",
+            "t_us": tu_us, "tflops": flops / (tu_us * 1e-6) / 1e12,
+            "pct_bf16_peak": 100.0 * flops / (tu_us * 1e-6) / 1e12 / peaks["bf16_tflops"],
+            "t_post_only_fused_us": tuf_us, "load_side_overhead_us": tu_us - tuf_us,
+            "t_serial_us": tus_us, "serial": "3 x xs_a2a_permute_inverse + xs_attn_ws + xs_a2a_permute",
+            "speedup_vs_serial": tus_us / tu_us, "t_inverse_permute_us": ti_us,
+        },
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
                 "ms_per_step": e2e_max / args.steps},
         "gpu_launches": gpu_launches,

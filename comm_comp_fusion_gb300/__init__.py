@@ -11,6 +11,9 @@ device pointers. Shapes follow the C ABI:
     q, k, v  : head-partitioned     [P][B][S][H/P][D]  bf16
     out      : sequence-partitioned [P][B][S/P][H][D]  bf16   (attn_a2a, a2a_permute)
                head-partitioned     [P][B][S][H/P][D]  bf16   (attn)
+
+``ulysses_attn`` takes q, k, v and out all sequence-partitioned (both
+All-to-Alls fused); ``a2a_permute_inverse`` maps sequence- to head-partitioned.
 """
 from __future__ import annotations
 
@@ -33,8 +36,9 @@ STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIG
                 5: "XS_ERR_CUDA", 6: "XS_ERR_TIMEOUT", 7: "XS_ERR_ALIAS", 8: "XS_ERR_WORKSPACE"}
 
 # Every symbol include/xs.h declares.
-EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size",
-           "xs_attn_a2a_noalloc", "xs_last_error", "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
+EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_a2a_permute_inverse", "xs_ulysses_attn",
+           "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size", "xs_attn_a2a_noalloc", "xs_last_error",
+           "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
 
 
 class XsError(RuntimeError):
@@ -55,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.xs_a2a_permute.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.xs_a2a_permute.restype = i
     sz = ctypes.c_size_t
+    lib.xs_a2a_permute_inverse.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.xs_a2a_permute_inverse.restype = ctypes.c_int
+    lib.xs_ulysses_attn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_ulysses_attn.restype = ctypes.c_int
     lib.xs_attn_a2a_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_a2a_ws.restype = i
     lib.xs_attn_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
@@ -158,6 +166,21 @@ def attn_a2a_noalloc(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True
 def a2a_permute(inp, out, B, S, H, D, P, stream=None, check=True):
     """Standalone All-to-All layout pass (``xs_a2a_permute``); returns the status."""
     st = lib.xs_a2a_permute(_ptr(inp), _ptr(out), B, S, H, D, P, _stream(stream, inp, out))
+    return _check(st) if check else st
+
+
+def a2a_permute_inverse(inp, out, B, S, H, D, P, stream=None, check=True):
+    """Standalone pre-attention All-to-All, sequence- to head-partitioned
+    (``xs_a2a_permute_inverse``); returns the status."""
+    st = lib.xs_a2a_permute_inverse(_ptr(inp), _ptr(out), B, S, H, D, P, _stream(stream, inp, out))
+    return _check(st) if check else st
+
+
+def ulysses_attn(q, k, v, out, B, S, H, D, P, scale, workspace=None, workspace_bytes=None, stream=None, check=True):
+    """Attention with both Ulysses All-to-Alls fused (``xs_ulysses_attn``): q, k, v and
+    out sequence-partitioned; ``workspace=None`` selects the whole-item schedule."""
+    st = lib.xs_ulysses_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                             _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
     return _check(st) if check else st
 
 

@@ -139,15 +139,53 @@ xs_status make_head_map(CUtensorMap *m, const void *ptr, int B, int S, int H, in
     return XS_OK;
 }
 
+// Tensor map over rank r's slice [B][Sl][H][D] of a sequence-partitioned
+// tensor [P][B][Sl][H][D], box = 64 columns x `rows` tokens of one head
+// (`rows` divides Sl, so a box never crosses into the next rank's slice).
+xs_status make_rank_map(CUtensorMap *m, const void *ptr, int r, int B, int S, int H, int D, int P, int rows,
+                        const char *name) {
+    EncodeTiledFn enc;
+    xs_status st = get_encoder(&enc);
+    if (st) return st;
+    const int Sl = S / P;
+    const size_t slice = (size_t)B * Sl * H * D * 2;
+    void *base = static_cast<char *>(const_cast<void *>(ptr)) + (size_t)r * slice;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Sl, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)Sl * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(XS_ERR_CUDA, "cuTensorMapEncodeTiled(%s, rank %d) failed with CUresult %d", name, r, (int)res);
+    return XS_OK;
+}
+
+int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
 std::atomic<uint32_t> g_generation{1};
 
+// layout 0: q, k, v head-partitioned, out as `epi` says. layout 1: q, k, v and
+// out sequence-partitioned (both All-to-Alls fused; `epi` must be 1).
 xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
-                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0) {
+                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0, int layout = 0) {
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
     if (!std::isfinite(scale)) return fail(XS_ERR_SHAPE, "scale must be finite");
+    if (layout == 1) {
+        if (P > xs::kMaxRanks) return fail(XS_ERR_UNSUPPORTED, "P=%d exceeds the %d ranks supported", P, xs::kMaxRanks);
+        if ((S / P) % 8) return fail(XS_ERR_UNSUPPORTED, "S/P=%d tokens per rank is not a multiple of 8", S / P);
+    }
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return fail(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
     if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
@@ -168,12 +206,23 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         (st = check_device_pointer(v, dev, "v")) || (st = check_device_pointer(out, dev, "out")))
         return st;
 
-    CUtensorMap tq, tk, tv;
-    if ((st = make_head_map(&tq, q, B, S, H, D, P, "q")) || (st = make_head_map(&tk, k, B, S, H, D, P, "k")) ||
-        (st = make_head_map(&tv, v, B, S, H, D, P, "v")))
-        return st;
-
     xs::AttnParams p;
+    p.ld_rows = gcd_int(S / P, 128);
+    xs::OperandMaps<1> head_maps;
+    xs::OperandMaps<xs::kMaxRanks> rank_maps;
+    if (layout == 0) {
+        if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q")) ||
+            (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k")) ||
+            (st = make_head_map(&head_maps.v[0], v, B, S, H, D, P, "v")))
+            return st;
+    } else {
+        memset(&rank_maps, 0, sizeof rank_maps);
+        for (int r = 0; r < P; ++r)
+            if ((st = make_rank_map(&rank_maps.q[r], q, r, B, S, H, D, P, p.ld_rows, "q")) ||
+                (st = make_rank_map(&rank_maps.k[r], k, r, B, S, H, D, P, p.ld_rows, "k")) ||
+                (st = make_rank_map(&rank_maps.v[r], v, r, B, S, H, D, P, p.ld_rows, "v")))
+                return st;
+    }
     p.B = B;
     p.S = S;
     p.H = H;
@@ -202,7 +251,9 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         p.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
     }
     const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr);
-    cudaError_t e = xs::launch_attention(D, epi, tq, tk, tv, p, grid, static_cast<cudaStream_t>(stream));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
+                                : xs::launch_ulysses(D, rank_maps, p, grid, s);
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
     return XS_OK;
 }
@@ -237,6 +288,11 @@ xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int
     return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0, workspace, workspace_bytes);
 }
 
+xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                          float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes, 1);
+}
+
 xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *bytes) {
     if (!bytes) return fail(XS_ERR_NULL, "bytes must be non-NULL");
     size_t tb = 0;
@@ -254,7 +310,11 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
     return XS_OK;
 }
 
-xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream) {
+}  // extern "C"
+
+namespace {
+
+xs_status permute_call(const void *in, void *out, int B, int S, int H, int D, int P, void *stream, bool inverse) {
     if (!in || !out) return fail(XS_ERR_NULL, "in and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, false, &bytes);
@@ -279,9 +339,22 @@ xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, 
     xs::fastdiv_magic(p.Sl, &p.mSl, &p.sSl);
     xs::fastdiv_magic(p.B, &p.mB, &p.sB);
     xs::fastdiv_magic(p.Hl, &p.mHl, &p.sHl);
-    cudaError_t e = xs::launch_permute(in, out, p, info.num_sms, static_cast<cudaStream_t>(stream));
+    xs::fastdiv_magic(p.S, &p.mS, &p.sS);
+    cudaError_t e = xs::launch_permute(in, out, p, inverse, info.num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda("permute launch", e);
     return XS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream) {
+    return permute_call(in, out, B, S, H, D, P, stream, false);
+}
+
+xs_status xs_a2a_permute_inverse(const void *in, void *out, int B, int S, int H, int D, int P, void *stream) {
+    return permute_call(in, out, B, S, H, D, P, stream, true);
 }
 
 const char *xs_last_error(void) { return g_last_error.c_str(); }

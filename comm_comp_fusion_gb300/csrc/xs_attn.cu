@@ -11,7 +11,11 @@
 //     Q-loop runs while those stores drain; no warp or SM is reserved for
 //     communication;
 //   * section 4.3, Figure 5 (d-e): the destination is the Ulysses sequence
-//     partition: token s of global head h = r*Hl + hl goes to rank r' = s / Sl.
+//     partition: token s of global head h = r*Hl + hl goes to rank r' = s / Sl;
+//   * section 4.3, Figure 5 (a-c): optionally (LD = 1) the pre-attention
+//     All-to-All is folded into the loads too: Q, K and V rows of head h are
+//     fetched from the sequence-partitioned slices of the ranks that own them,
+//     through one TMA tensor map per rank.
 //
 // Softmax is computed online (running row max m, running sum l, rescaling of
 // O when m grows), in base 2 with scale*log2(e) folded into one FMA. The row
@@ -405,10 +409,41 @@ __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, 
 }
 
 
-template <int D, int EPI>
+// Issues the TMA copies of token rows [s0, s0 + 128) of one head of one operand
+// into a 128-row tile at shared address `dst` (D/64 swizzle blocks of 128 rows).
+// LD = 0: head-partitioned tensor, one 128-row box per block. LD = 1: the rows
+// are read where the sequence partition keeps them, in the slice of the rank
+// that owns each token (the pre-attention All-to-All of Ulysses, section 4.3,
+// Figure 5 (a-c)), through that rank's tensor map; the box height divides Sl,
+// so no box straddles two ranks. Rows at or past S (the absent second tile of
+// an odd tile count) lie outside every map and are zero-filled.
+template <int D, int LD>
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *maps, uint32_t bar, const AttnParams &p,
+                                          int rb, int hl, int s0) {
+    using C = Cfg<D>;
+    if (LD == 0) {
+#pragma unroll
+        for (int db = 0; db < C::kNDB; ++db) tma_load_4d(dst + db * C::kBlk, maps, bar, db * 64, hl, s0, rb);
+    } else {
+        const int b = rb % p.B, h = (rb / p.B) * p.Hl + hl;
+        int rs = s0 < p.S ? s0 / p.Sl : p.P - 1;  // rank holding token s0
+        int sl = s0 - rs * p.Sl;                  // its position in that rank's slice
+        for (int y = 0; y < 128; y += p.ld_rows) {
+#pragma unroll
+            for (int db = 0; db < C::kNDB; ++db)
+                tma_load_4d(dst + db * C::kBlk + (uint32_t)y * 128u, maps + rs, bar, db * 64, h, sl, b);
+            sl += p.ld_rows;
+            if (sl == p.Sl && rs + 1 < p.P) {
+                sl = 0;
+                ++rs;
+            }
+        }
+    }
+}
+
+template <int D, int EPI, int LD>
 __global__ void __launch_bounds__(512, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -442,9 +477,11 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(BAR(B_DRAIN), 1);
         misc[1] = 0u;
         fence_mbar_init();
-        prefetch_tmap(&tmq);
-        prefetch_tmap(&tmk);
-        prefetch_tmap(&tmv);
+        for (int r = 0; r < (LD ? p.P : 1); ++r) {
+            prefetch_tmap(&tm.q[r]);
+            prefetch_tmap(&tm.k[r]);
+            prefetch_tmap(&tm.v[r]);
+        }
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(misc), C::kTmemCols);
@@ -472,10 +509,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kTile);
                     const int s0 = (2 * w.pair + t) * 128;  // past S for an absent tile: zero fill
-#pragma unroll
-                    for (int db = 0; db < C::kNDB; ++db)
-                        tma_load_4d(sQ + t * C::kTile + db * C::kBlk, &tmq, BAR(BQ_FULL + t), db * 64, w.hl, s0,
-                                    w.rb);
+                    load_rows<D, LD>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), p, w.rb, w.hl, s0);
                 }
                 for (int j = g.j0; ok && j < g.j1; ++j) {
                     for (int kv = 0; kv < 2; ++kv, ++kv_it) {
@@ -483,11 +517,8 @@ __global__ void __launch_bounds__(512, 1)
                         ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
                         if (!ok) break;
                         mbar_arrive_expect_tx(BAR(BKV_FULL + slot), C::kTile);
-                        const CUtensorMap *m = kv ? &tmv : &tmk;
-#pragma unroll
-                        for (int db = 0; db < C::kNDB; ++db)
-                            tma_load_4d(sKV + slot * C::kTile + db * C::kBlk, m, BAR(BKV_FULL + slot), db * 64,
-                                        w.hl, j * 128, w.rb);
+                        load_rows<D, LD>(sKV + slot * C::kTile, kv ? tm.v : tm.k, BAR(BKV_FULL + slot), p, w.rb,
+                                         w.hl, j * 128);
                     }
                 }
             }
@@ -851,20 +882,27 @@ size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     return rec + cnt;
 }
 
-template <int D, int EPI>
-static cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const AttnParams &p, int grid, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI>;
+template <int D, int EPI, int LD>
+static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
+                            cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, EPI, LD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p);
+    kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention(int D, int epi, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const AttnParams &p, int grid, cudaStream_t stream) {
-    if (D == 128) return epi ? launch_t<128, 1>(tq, tk, tv, p, grid, stream) : launch_t<128, 0>(tq, tk, tv, p, grid, stream);
-    if (D == 64) return epi ? launch_t<64, 1>(tq, tk, tv, p, grid, stream) : launch_t<64, 0>(tq, tk, tv, p, grid, stream);
+cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                             cudaStream_t stream) {
+    if (D == 128) return epi ? launch_t<128, 1, 0>(maps, p, grid, stream) : launch_t<128, 0, 0>(maps, p, grid, stream);
+    if (D == 64) return epi ? launch_t<64, 1, 0>(maps, p, grid, stream) : launch_t<64, 0, 0>(maps, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
+                           cudaStream_t stream) {
+    if (D == 128) return launch_t<128, 1, 1>(maps, p, grid, stream);
+    if (D == 64) return launch_t<64, 1, 1>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

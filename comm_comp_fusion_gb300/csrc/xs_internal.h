@@ -20,6 +20,7 @@ namespace xs {
 // ranges is computed in pieces whose partial results meet in the workspace.
 struct AttnParams {
     int B, S, H, P, Hl, Sl;
+    int ld_rows;  // sequence-partitioned inputs: token rows per TMA box (gcd(Sl, 128))
     int n_qt;     // 128-row query tiles per head  (S / 128)
     int n_pairs;  // work items per head           (ceil(n_qt / 2))
     int n_kv;     // 128-row K/V tiles per head    (S / 128)
@@ -45,9 +46,24 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced);
 // Workspace bytes a balanced call needs (records, then counters), 256-aligned parts.
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms);
 
+// Most simulated ranks a call with sequence-partitioned inputs accepts: the
+// kernel takes one TMA tensor map per source rank and operand as a parameter.
+constexpr int kMaxRanks = 8;
+
+// TMA tensor maps of Q, K and V. NM = 1: one map per operand over the
+// head-partitioned tensor. NM = kMaxRanks: one map per source rank over that
+// rank's sequence-partitioned slice (entries past P unused).
+template <int NM> struct OperandMaps {
+    CUtensorMap q[NM], k[NM], v[NM];
+};
+
 // epi = 0: head-partitioned output (same layout as q); epi = 1: All-to-All scatter.
-cudaError_t launch_attention(int D, int epi, const CUtensorMap &tq, const CUtensorMap &tk,
-                             const CUtensorMap &tv, const AttnParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                             cudaStream_t stream);
+// Sequence-partitioned inputs (the pre-attention All-to-All done by the loads),
+// sequence-partitioned output.
+cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
+                           cudaStream_t stream);
 
 // Sets the calling thread's xs_last_error() text; returns `status`.
 int report_error(int status, const char *message);
@@ -60,10 +76,13 @@ struct PermParams {
     uint32_t rows;       // B * S * H rows of D elements
     uint32_t cpr_log2;   // log2(16-byte chunks per row)
     uint32_t B, S, H, Hl, Sl;
-    // magic numbers for division by H, Sl, B and Hl (round-up method)
-    uint32_t mH, sH, mSl, sSl, mB, sB, mHl, sHl;
+    // magic numbers for division by H, Sl, B, Hl and S (round-up method)
+    uint32_t mH, sH, mSl, sSl, mB, sB, mHl, sHl, mS, sS;
 };
 void fastdiv_magic(uint32_t d, uint32_t *m, uint32_t *s);
-cudaError_t launch_permute(const void *in, void *out, const PermParams &p, int num_sms, cudaStream_t stream);
+// inverse = false: head-partitioned -> sequence-partitioned (post-attention
+// All-to-All); inverse = true: the reverse (pre-attention All-to-All).
+cudaError_t launch_permute(const void *in, void *out, const PermParams &p, bool inverse, int num_sms,
+                           cudaStream_t stream);
 
 }  // namespace xs

@@ -1,12 +1,15 @@
-// xs_permute.cu -- the standalone post-attention All-to-All of Ulysses sequence
-// parallelism on one GPU (X-Stage paper, arXiv 2607.23264v1, section 4.3,
-// Figure 5 (d-e); the "A2A-only" variant and second half of "Serial" in
-// section 5.3): head-partitioned [P][B][S][Hl][D] -> sequence-partitioned
-// [P][B][Sl][H][D]. Every row of D elements moves whole, so the kernel is an
-// HBM-bound gather of 16-byte chunks: threads walk the OUTPUT in order (so
-// stores are fully coalesced) and fetch each chunk from its source row.
-// Index arithmetic uses precomputed multiply-shift division (Granlund and
-// Montgomery, "Division by Invariant Integers using Multiplication", 1994).
+// xs_permute.cu -- the standalone All-to-Alls of Ulysses sequence parallelism
+// on one GPU (X-Stage paper, arXiv 2607.23264v1, section 4.3, Figure 5; the
+// "A2A-only" variant and the All-to-All half of "Serial" in section 5.3):
+//   forward: head-partitioned [P][B][S][Hl][D] -> sequence-partitioned
+//            [P][B][Sl][H][D] (the post-attention All-to-All, Figure 5 (d-e));
+//   inverse: sequence-partitioned -> head-partitioned (the pre-attention
+//            All-to-All, Figure 5 (a-c)).
+// Every row of D elements moves whole, so each direction is an HBM-bound
+// gather of 16-byte chunks: threads walk the OUTPUT in order (so stores are
+// fully coalesced) and fetch each chunk from its source row. Index arithmetic
+// uses precomputed multiply-shift division (Granlund and Montgomery, "Division
+// by Invariant Integers using Multiplication", 1994).
 #include "xs_internal.h"
 
 namespace xs {
@@ -23,7 +26,21 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, uint32_t m, uint32_t s) {
     return (__umulhi(n, m) + n) >> s;
 }
 
+template <bool INV>
 __device__ __forceinline__ uint32_t src_chunk_row(uint32_t orow, const PermParams &p) {
+    if (INV) {
+        // output row orow = ((r * B + b) * S + s) * Hl + hl
+        const uint32_t t1 = fdiv(orow, p.mHl, p.sHl);
+        const uint32_t hl = orow - t1 * p.Hl;
+        const uint32_t t2 = fdiv(t1, p.mS, p.sS);
+        const uint32_t s = t1 - t2 * p.S;
+        const uint32_t r = fdiv(t2, p.mB, p.sB);
+        const uint32_t b = t2 - r * p.B;
+        const uint32_t rd = fdiv(s, p.mSl, p.sSl);
+        const uint32_t sl = s - rd * p.Sl;
+        // source row ((rd * B + b) * Sl + sl) * H + r * Hl + hl
+        return ((rd * p.B + b) * p.Sl + sl) * p.H + r * p.Hl + hl;
+    }
     // output row orow = ((rd * B + b) * Sl + sl) * H + h
     const uint32_t t1 = fdiv(orow, p.mH, p.sH);
     const uint32_t h = orow - t1 * p.H;
@@ -49,6 +66,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *ptr) {
 constexpr int kPermThreads = 256;
 constexpr int kPermUnroll = 4;
 
+template <bool INV>
 __global__ void __launch_bounds__(kPermThreads) a2a_permute_kernel(const uint4 *__restrict__ in,
                                                                    uint4 *__restrict__ out, const PermParams p) {
     const uint64_t total = (uint64_t)p.rows << p.cpr_log2;
@@ -61,7 +79,7 @@ __global__ void __launch_bounds__(kPermThreads) a2a_permute_kernel(const uint4 *
         for (int u = 0; u < kPermUnroll; ++u) {
             const uint64_t o = i + u * stride;
             const uint32_t orow = (uint32_t)(o >> p.cpr_log2);
-            const uint64_t src = ((uint64_t)src_chunk_row(orow, p) << p.cpr_log2) | (o & cmask);
+            const uint64_t src = ((uint64_t)src_chunk_row<INV>(orow, p) << p.cpr_log2) | (o & cmask);
             v[u] = ld_stream(in + src);
         }
 #pragma unroll
@@ -69,19 +87,20 @@ __global__ void __launch_bounds__(kPermThreads) a2a_permute_kernel(const uint4 *
     }
     for (; i < total; i += stride) {
         const uint32_t orow = (uint32_t)(i >> p.cpr_log2);
-        const uint64_t src = ((uint64_t)src_chunk_row(orow, p) << p.cpr_log2) | (i & cmask);
+        const uint64_t src = ((uint64_t)src_chunk_row<INV>(orow, p) << p.cpr_log2) | (i & cmask);
         out[i] = ld_stream(in + src);
     }
 }
 
-cudaError_t launch_permute(const void *in, void *out, const PermParams &p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_permute(const void *in, void *out, const PermParams &p, bool inverse, int num_sms,
+                           cudaStream_t stream) {
     const uint64_t total = (uint64_t)p.rows << p.cpr_log2;
     uint64_t blocks = (total + kPermThreads - 1) / kPermThreads;
     const uint64_t cap = (uint64_t)num_sms * (2048 / kPermThreads);  // one full wave of resident threads
     if (blocks > cap) blocks = cap;
     if (blocks == 0) return cudaSuccess;
-    a2a_permute_kernel<<<(unsigned)blocks, kPermThreads, 0, stream>>>(static_cast<const uint4 *>(in),
-                                                                      static_cast<uint4 *>(out), p);
+    auto kern = inverse ? a2a_permute_kernel<true> : a2a_permute_kernel<false>;
+    kern<<<(unsigned)blocks, kPermThreads, 0, stream>>>(static_cast<const uint4 *>(in), static_cast<uint4 *>(out), p);
     return cudaGetLastError();
 }
 

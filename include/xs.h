@@ -14,6 +14,9 @@
  *   - Section 5.3: "FA-only" (xs_attn), "A2A-only" (xs_a2a_permute), "Serial"
  *     (xs_attn then xs_a2a_permute) and "Fused" (xs_attn_a2a) are the four
  *     compared implementations.
+ *   - Section 4.3, Figure 5 (a-c): before attention a first All-to-All turns
+ *     the sequence partition into the head partition (xs_a2a_permute_inverse);
+ *     xs_ulysses_attn folds it into the attention kernel's loads.
  *
  * Ranks. P ranks are simulated as P contiguous slices of one allocation on the
  * calling GPU, so the All-to-All is a scatter of rows into slices; nothing
@@ -100,6 +103,35 @@ xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B,
  * S % P == 0 (no multiple-of-128 rule). in and out must not overlap.
  */
 xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream);
+
+/*
+ * Standalone pre-attention All-to-All (Ulysses, section 4.3, Figure 5 (a-c)):
+ * the inverse of xs_a2a_permute.
+ *   in  : sequence-partitioned [P][B][Sl][H][D], 16-bit elements (any payload).
+ *   out : head-partitioned [P][B][S][Hl][D], fully overwritten.
+ * A pure copy; xs_a2a_permute(xs_a2a_permute_inverse(x)) == x bit for bit.
+ * Shape and pointer rules as for xs_a2a_permute.
+ */
+xs_status xs_a2a_permute_inverse(const void *in, void *out, int B, int S, int H, int D, int P, void *stream);
+
+/*
+ * Both Ulysses All-to-Alls fused into one attention call (section 4.3,
+ * Figure 5 (a-e), with the output side of Figure 7): attention over the whole
+ * sequence for every head, from and to the sequence partition.
+ *   q, k, v : sequence-partitioned [P][B][Sl][H][D] bf16, read only. Each
+ *             128-row tile of head h is loaded where the sequence partition
+ *             keeps it, from the slices of the ranks that own its tokens (one
+ *             TMA tensor map per rank and operand), so no head-partitioned
+ *             copy is ever made.
+ *   out     : sequence-partitioned [P][B][Sl][H][D] bf16, fully overwritten.
+ *   workspace, workspace_bytes : as for xs_attn_a2a_ws (NULL, 0: whole-item
+ *             schedule); the size is xs_attn_workspace_size's.
+ * Bit-identical to xs_attn_a2a_ws(xs_a2a_permute_inverse(q), ...(k), ...(v))
+ * with the same workspace choice. Extra rules: P <= 8 and S/P % 8 == 0
+ * (XS_ERR_UNSUPPORTED otherwise).
+ */
+xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                          int P, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Balanced-schedule variants. Identical results contract and layouts as

@@ -94,6 +94,24 @@ def test_workspace_argument_checks(xs):
     assert xs.lib.xs_attn_workspace_size(1, 256, 8, 64, 4, None) == xs.XS_ERR_NULL
 
 
+def test_ulysses_argument_checks(xs):
+    W = 0x50000000
+    f = lambda q=Q, o=O, ws=None, nb=0, **kw: xs.ulysses_attn(
+        q, K, V, o, kw.get("B", 1), kw.get("S", 256), kw.get("H", 8), kw.get("D", 64), kw.get("P", 4),
+        kw.get("scale", 0.125), ws, nb, check=False)
+    assert f(q=0) == xs.XS_ERR_NULL
+    assert f(H=6) == xs.XS_ERR_SHAPE
+    assert f(S=200) == xs.XS_ERR_SHAPE
+    assert f(D=96) == xs.XS_ERR_UNSUPPORTED
+    assert f(P=16, H=16) == xs.XS_ERR_UNSUPPORTED and "P=16" in xs.last_error()
+    assert f(o=Q + 32) == xs.XS_ERR_ALIAS
+    assert f(o=O + 8) == xs.XS_ERR_ALIGN
+    assert f(ws=None, nb=64) == xs.XS_ERR_WORKSPACE
+    assert f(ws=W + 64, nb=1 << 20) == xs.XS_ERR_WORKSPACE
+    assert f(B=0) == xs.XS_OK
+    assert f(S=0, P=16, H=16) == xs.XS_ERR_UNSUPPORTED   # the rank limit holds for empty calls too
+
+
 def test_permute_argument_checks(xs):
     f = lambda i=Q, o=O, B=1, S=256, H=8, D=64, P=4: xs.a2a_permute(i, o, B, S, H, D, P, check=False)
     assert f(i=0) == xs.XS_ERR_NULL
@@ -104,6 +122,12 @@ def test_permute_argument_checks(xs):
     assert f(o=Q + 16) == xs.XS_ERR_ALIAS
     assert f(B=0) == xs.XS_OK
     assert f(S=4, P=2) != xs.XS_ERR_SHAPE   # no multiple-of-128 rule for the permute
+    g = lambda i=Q, o=O, B=1, S=256, H=8, D=64, P=4: xs.a2a_permute_inverse(i, o, B, S, H, D, P, check=False)
+    assert g(o=0) == xs.XS_ERR_NULL
+    assert g(S=6, P=4) == xs.XS_ERR_SHAPE
+    assert g(i=Q + 2) == xs.XS_ERR_ALIGN
+    assert g(o=Q - 16) == xs.XS_ERR_ALIAS
+    assert g(B=0) == xs.XS_OK
 
 
 def test_selftest_rejects_bad_limit(xs):
