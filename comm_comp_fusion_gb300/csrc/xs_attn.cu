@@ -411,34 +411,40 @@ __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, 
 
 // Issues the TMA copies of token rows [s0, s0 + 128) of one head of one operand
 // into a 128-row tile at shared address `dst` (D/64 swizzle blocks of 128 rows).
-// LD = 0: head-partitioned tensor, one 128-row box per block. LD = 1: the rows
-// are read where the sequence partition keeps them, in the slice of the rank
-// that owns each token (the pre-attention All-to-All of Ulysses, section 4.3,
-// Figure 5 (a-c)), through that rank's tensor map; the box height divides Sl,
-// so no box straddles two ranks. Rows at or past S (the absent second tile of
-// an odd tile count) lie outside every map and are zero-filled.
-template <int D, int LD>
-__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *maps, uint32_t bar, const AttnParams &p,
-                                          int rb, int hl, int s0) {
-    using C = Cfg<D>;
-    if (LD == 0) {
+// Head-partitioned tensor: one 128-row box per block.
+template <int D>
+__device__ __forceinline__ void load_rows_head(uint32_t dst, const CUtensorMap *map, uint32_t bar, int rb, int hl,
+                                               int s0) {
 #pragma unroll
-        for (int db = 0; db < C::kNDB; ++db) tma_load_4d(dst + db * C::kBlk, maps, bar, db * 64, hl, s0, rb);
-    } else {
-        const int b = rb % p.B, h = (rb / p.B) * p.Hl + hl;
-        int rs = s0 < p.S ? s0 / p.Sl : p.P - 1;  // rank holding token s0
-        int sl = s0 - rs * p.Sl;                  // its position in that rank's slice
-        for (int y = 0; y < 128; y += p.ld_rows) {
+    for (int db = 0; db < Cfg<D>::kNDB; ++db) tma_load_4d(dst + db * Cfg<D>::kBlk, map, bar, db * 64, hl, s0, rb);
+}
+
+// Sequence-partitioned tensor: the rows are read where the sequence partition
+// keeps them, in the slice of the rank that owns each token (the pre-attention
+// All-to-All of Ulysses, section 4.3, Figure 5 (a-c)), through that rank's
+// tensor map. Token s0 is row `sl` of rank `rs`'s slice; the box height
+// p.ld_rows divides Sl, so no box straddles two ranks. Rows at or past S (the
+// absent second tile of an odd tile count) lie outside every map and are
+// zero-filled.
+template <int D>
+__device__ __forceinline__ void load_rows_seq(uint32_t dst, const CUtensorMap *maps, uint32_t bar,
+                                              const AttnParams &p, int b, int h, int rs, int sl) {
+    for (int y = 0; y < 128; y += p.ld_rows) {
 #pragma unroll
-            for (int db = 0; db < C::kNDB; ++db)
-                tma_load_4d(dst + db * C::kBlk + (uint32_t)y * 128u, maps + rs, bar, db * 64, h, sl, b);
-            sl += p.ld_rows;
-            if (sl == p.Sl && rs + 1 < p.P) {
-                sl = 0;
-                ++rs;
-            }
+        for (int db = 0; db < Cfg<D>::kNDB; ++db)
+            tma_load_4d(dst + db * Cfg<D>::kBlk + (uint32_t)y * 128u, maps + rs, bar, db * 64, h, sl, b);
+        sl += p.ld_rows;
+        if (sl == p.Sl && rs + 1 < p.P) {
+            sl = 0;
+            ++rs;
         }
     }
+}
+
+// Rank holding token s (the last rank for s >= S) and its row in that slice.
+__device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs, int &sl) {
+    rs = s < p.S ? s / p.Sl : p.P - 1;
+    sl = s - rs * p.Sl;
 }
 
 template <int D, int EPI, int LD>
@@ -504,21 +510,41 @@ __global__ void __launch_bounds__(512, 1)
             Seg g;
             for (; ok && sched_next(sch, p, g); ++it) {
                 const Item w = decode_item(p, g.item);
+                // sequence-partitioned inputs: batch and global head of the item
+                const int b = LD ? w.rb % p.B : 0, h = LD ? (w.rb / p.B) * p.Hl + w.hl : 0;
                 for (int t = 0; t < 2 && ok; ++t) {
                     ok = bwait(BAR(BQ_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteLoadQ);
                     if (!ok) break;
                     mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kTile);
                     const int s0 = (2 * w.pair + t) * 128;  // past S for an absent tile: zero fill
-                    load_rows<D, LD>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), p, w.rb, w.hl, s0);
+                    if (LD) {
+                        int rs, sl;
+                        seq_position(p, s0, rs, sl);
+                        load_rows_seq<D>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), p, b, h, rs, sl);
+                    } else {
+                        load_rows_head<D>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), w.rb, w.hl, s0);
+                    }
                 }
+                int rs = 0, sl = 0;  // position of K/V token j * 128, advanced tile by tile
+                if (LD) seq_position(p, g.j0 * 128, rs, sl);
                 for (int j = g.j0; ok && j < g.j1; ++j) {
                     for (int kv = 0; kv < 2; ++kv, ++kv_it) {
                         const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u;
                         ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
                         if (!ok) break;
                         mbar_arrive_expect_tx(BAR(BKV_FULL + slot), C::kTile);
-                        load_rows<D, LD>(sKV + slot * C::kTile, kv ? tm.v : tm.k, BAR(BKV_FULL + slot), p, w.rb,
-                                         w.hl, j * 128);
+                        const CUtensorMap *m = kv ? tm.v : tm.k;
+                        if (LD)
+                            load_rows_seq<D>(sKV + slot * C::kTile, m, BAR(BKV_FULL + slot), p, b, h, rs, sl);
+                        else
+                            load_rows_head<D>(sKV + slot * C::kTile, m, BAR(BKV_FULL + slot), w.rb, w.hl, j * 128);
+                    }
+                    if (LD) {
+                        sl += 128;
+                        while (sl >= p.Sl && rs + 1 < p.P) {
+                            sl -= p.Sl;
+                            ++rs;
+                        }
                     }
                 }
             }
