@@ -35,16 +35,25 @@ XS_ERR_WORKSPACE = 8
 STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIGN", 4: "XS_ERR_UNSUPPORTED",
                 5: "XS_ERR_CUDA", 6: "XS_ERR_TIMEOUT", 7: "XS_ERR_ALIAS", 8: "XS_ERR_WORKSPACE"}
 
-# Every symbol include/xs.h declares.
+# Every symbol include/*.h declares.
 EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_a2a_permute_inverse", "xs_ulysses_attn",
            "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size", "xs_attn_a2a_noalloc", "xs_last_error",
-           "xs_device_status", "xs_selftest_wait_timeout", "xs_version")
+           "xs_device_status", "xs_selftest_wait_timeout", "xs_version", "xs_attn_a2a_trace", "xs_attn_trace_layout",
+           # include/xs_burst.h
+           "xs_burst_rec_bytes", "xs_burst_gap")
 
 
 class XsError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
         self.status = status
+
+
+class BurstStats(ctypes.Structure):
+    """xs_burst_stats of include/xs_burst.h."""
+    _fields_ = [("t_iss_mean_ns", ctypes.c_double), ("t_iss_max_ns", ctypes.c_double),
+                ("t_period_ns", ctypes.c_double), ("sm_clock_mhz", ctypes.c_double),
+                ("bursts_measured", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -63,6 +72,14 @@ def _load() -> ctypes.CDLL:
     lib.xs_a2a_permute_inverse.restype = ctypes.c_int
     lib.xs_ulysses_attn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_ulysses_attn.restype = ctypes.c_int
+    lib.xs_attn_a2a_trace.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_a2a_trace.restype = i
+    lib.xs_attn_trace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(sz)]
+    lib.xs_attn_trace_layout.restype = i
+    lib.xs_burst_rec_bytes.argtypes = [i, i]
+    lib.xs_burst_rec_bytes.restype = sz
+    lib.xs_burst_gap.argtypes = [vp, sz, vp, sz, i, i, i, ctypes.c_double, i, i, i, i, ctypes.POINTER(BurstStats), vp]
+    lib.xs_burst_gap.restype = ctypes.c_int
     lib.xs_attn_a2a_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_a2a_ws.restype = i
     lib.xs_attn_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
@@ -182,6 +199,35 @@ def ulysses_attn(q, k, v, out, B, S, H, D, P, scale, workspace=None, workspace_b
     st = lib.xs_ulysses_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
                              _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
     return _check(st) if check else st
+
+
+def attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, trace, trace_bytes=None, stream=None, check=True):
+    """Fused call with the epilogue traced (``xs_attn_a2a_trace``); returns the status."""
+    st = lib.xs_attn_a2a_trace(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(trace),
+                               _nbytes(trace, trace_bytes), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def trace_layout(B, S, H, D, P):
+    """``xs_attn_trace_layout``: (ctas, items_per_cta, trace bytes) on the current device."""
+    c, n, b = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(lib.xs_attn_trace_layout(B, S, H, D, P, ctypes.byref(c), ctypes.byref(n), ctypes.byref(b)))
+    return c.value, n.value, b.value
+
+
+def burst_gap(buf, buf_bytes, rec, rec_bytes, K, B, gap_ns, n_bursts, isolated=False, row_bytes=128,
+              row_stride=128, warps=4, stream=None):
+    """One Burst-Gap microbenchmark launch (``xs_burst_gap``); synchronises and returns
+    a dict with t_iss_mean_ns, t_iss_max_ns, t_period_ns, sm_clock_mhz, bursts_measured."""
+    st = BurstStats()
+    _check(lib.xs_burst_gap(_ptr(buf), int(buf_bytes), _ptr(rec), int(rec_bytes), K, warps, B, float(gap_ns),
+                            n_bursts, 1 if isolated else 0, row_bytes, row_stride, ctypes.byref(st),
+                            _stream(stream, buf)))
+    return {f: getattr(st, f) for f, _ in BurstStats._fields_}
+
+
+def burst_rec_bytes(K, n_bursts) -> int:
+    return lib.xs_burst_rec_bytes(K, n_bursts)
 
 
 def device_status(stream=None, clear=True) -> int:

@@ -176,12 +176,17 @@ std::atomic<uint32_t> g_generation{1};
 // layout 0: q, k, v head-partitioned, out as `epi` says. layout 1: q, k, v and
 // out sequence-partitioned (both All-to-Alls fused; `epi` must be 1).
 xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
-                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0, int layout = 0) {
+                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0, int layout = 0,
+                         void *trace = nullptr, size_t trace_bytes = 0) {
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
     if (!std::isfinite(scale)) return fail(XS_ERR_SHAPE, "scale must be finite");
+    if (trace) {
+        if (D != 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing is built for D=128 only (got D=%d)", D);
+        if (misaligned(trace)) return fail(XS_ERR_ALIGN, "trace must be 16-byte aligned");
+    }
     if (layout == 1) {
         if (P > xs::kMaxRanks) return fail(XS_ERR_UNSUPPORTED, "P=%d exceeds the %d ranks supported", P, xs::kMaxRanks);
         if ((S / P) % 8) return fail(XS_ERR_UNSUPPORTED, "S/P=%d tokens per rank is not a multiple of 8", S / P);
@@ -240,6 +245,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     p.ws_rec = nullptr;
     p.ws_cnt = nullptr;
     p.gen = 0;
+    p.trace = static_cast<unsigned long long *>(trace);
     if (ws) {
         const size_t need = xs::attn_workspace_bytes(p.n_items, p.n_kv, D, info.num_sms);
         if (ws_bytes < need)
@@ -252,6 +258,17 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     }
     const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (trace) {
+        const size_t need = (size_t)grid * p.n_dp * 8 * xs::kTraceWords * 8;
+        if (trace_bytes < need)
+            return fail(XS_ERR_SHAPE, "trace buffer of %zu bytes is smaller than the %zu bytes needed", trace_bytes,
+                        need);
+        if ((st = check_device_pointer(trace, dev, "trace"))) return st;
+        cudaError_t e = cudaMemsetAsync(trace, 0, need, s);
+        if (e == cudaSuccess) e = xs::launch_attention_traced(D, head_maps, p, grid, s);
+        if (e != cudaSuccess) return fail_cuda("traced attention launch", e);
+        return XS_OK;
+    }
     cudaError_t e = layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
                                 : xs::launch_ulysses(D, rank_maps, p, grid, s);
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
@@ -291,6 +308,37 @@ xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int
 xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                           float scale, void *workspace, size_t workspace_bytes, void *stream) {
     return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes, 1);
+}
+
+xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                            int P, float scale, void *trace, size_t trace_bytes, void *stream) {
+    if (!trace) return fail(XS_ERR_NULL, "trace must be non-NULL");
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, nullptr, 0, 0, trace, trace_bytes);
+}
+
+xs_status xs_attn_trace_layout(int B, int S, int H, int D, int P, int *ctas, int *items_per_cta, size_t *bytes) {
+    if (!ctas || !items_per_cta || !bytes) return fail(XS_ERR_NULL, "ctas, items_per_cta and bytes must be non-NULL");
+    size_t tb = 0;
+    xs_status st = check_shape(B, S, H, D, P, true, &tb);
+    if (st) return st;
+    if (tb == 0) {
+        *ctas = *items_per_cta = 0;
+        *bytes = 0;
+        return XS_OK;
+    }
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info))) return st;
+    xs::AttnParams p;
+    p.n_qt = S / 128;
+    p.n_pairs = (p.n_qt + 1) / 2;
+    p.n_kv = S / 128;
+    p.n_items = P * B * (H / P) * p.n_pairs;
+    const int grid = xs::attn_schedule(p, info.num_sms, false);
+    *ctas = grid;
+    *items_per_cta = p.n_dp;
+    *bytes = (size_t)grid * p.n_dp * 8 * xs::kTraceWords * 8;
+    return XS_OK;
 }
 
 xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *bytes) {

@@ -447,7 +447,7 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD>
+template <int D, int EPI, int LD, int TRACE>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
@@ -832,6 +832,11 @@ __global__ void __launch_bounds__(512, 1)
                     continue;
                 }
                 const float inv_l = 1.0f / l;
+                unsigned long long t_ready = 0, t_store = 0, g_ready = 0;
+                if (TRACE) {
+                    t_ready = clock64_now();
+                    g_ready = globaltimer_ns();
+                }
 #pragma unroll 1
                 for (int db = 0; db < C::kNDB; ++db) {
                     uint32_t o[64];
@@ -844,7 +849,18 @@ __global__ void __launch_bounds__(512, 1)
                                     pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
+                    if (TRACE && db == 0) t_store = clock64_now();
                     flush_block(p.out, stage, lane, dst, db);
+                }
+                if (TRACE && lane == 0) {
+                    const unsigned long long t_end = clock64_now();
+                    unsigned long long *r =
+                        p.trace + (((size_t)blockIdx.x * p.n_dp + it) * 8 + t * 4 + wq) * kTraceWords;
+                    r[0] = t_ready;
+                    r[1] = valid ? t_store : t_end;
+                    r[2] = t_end;
+                    r[3] = g_ready;
+                    r[4] = ((unsigned long long)g.item << 8) | (uint32_t)(t << 4) | (valid ? 0u : 8u) | (uint32_t)wq;
                 }
             }
             if (!ok || !pending) continue;
@@ -908,10 +924,10 @@ size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     return rec + cnt;
 }
 
-template <int D, int EPI, int LD>
+template <int D, int EPI, int LD, int TRACE = 0>
 static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
                             cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD>;
+    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
@@ -922,6 +938,12 @@ cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const A
                              cudaStream_t stream) {
     if (D == 128) return epi ? launch_t<128, 1, 0>(maps, p, grid, stream) : launch_t<128, 0, 0>(maps, p, grid, stream);
     if (D == 64) return epi ? launch_t<64, 1, 0>(maps, p, grid, stream) : launch_t<64, 0, 0>(maps, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                                    cudaStream_t stream) {
+    if (D == 128) return launch_t<128, 1, 0, 1>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

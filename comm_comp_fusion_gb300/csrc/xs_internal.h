@@ -34,7 +34,14 @@ struct AttnParams {
     float *ws_rec;         // 2 * G partial records (see partial_record_bytes)
     uint32_t *ws_cnt;      // 8 arrival counters per item of the balanced region
     uint32_t gen;          // generation stamped into the counters by this call
+    unsigned long long *trace;  // traced instances: epilogue records, kTraceWords per (CTA, item, tile, warp)
 };
+
+// Epilogue trace record of one output tile and epilogue warp (32 rows):
+// clock64 when the tile's O and row sums were ready, before its first store,
+// after its last store was issued; %globaltimer when ready; then
+// item << 8 | tile << 4 | warp, with bit 3 set for an absent tile.
+constexpr int kTraceWords = 5;
 
 // Bytes of one partial record: unnormalised O of both tiles (fp32) plus the
 // row max and row sum of both tiles.
@@ -60,6 +67,9 @@ template <int NM> struct OperandMaps {
 // epi = 0: head-partitioned output (same layout as q); epi = 1: All-to-All scatter.
 cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                              cudaStream_t stream);
+// The fused call with epilogue tracing (p.trace set, whole-item schedule).
+cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                                    cudaStream_t stream);
 // Sequence-partitioned inputs (the pre-attention All-to-All done by the loads),
 // sequence-partitioned output.
 cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,

@@ -19,6 +19,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+__device__ __forceinline__ unsigned long long clock64_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t)::"memory");
+    return t;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));

@@ -184,6 +184,29 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
 xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void *out, int B, int S, int H,
                               int D, int P, float scale, void *stream);
 
+/*
+ * The fused call (xs_attn_a2a, whole-item schedule) with its epilogue traced:
+ * the per-tile record the paper's section 5.2.3 uses to measure each output
+ * tile's sender-visible store span, and the section 4.3 audit its Q-loop gap.
+ * Results are bit-identical to xs_attn_a2a; the records cost a few clock reads
+ * and one 40-byte store per tile and epilogue warp. D = 128 only
+ * (XS_ERR_UNSUPPORTED otherwise).
+ *   trace, trace_bytes : device buffer of at least the size xs_attn_trace_layout
+ *       reports, 16-byte aligned; zeroed and then filled by the call. Layout:
+ *       [ctas][items_per_cta][tile 0..1][epilogue warp 0..3] records of five
+ *       uint64: clock64 when the tile's O and row sums were ready, clock64 just
+ *       before its first global store, clock64 after its last store was issued,
+ *       %globaltimer (ns) when ready, and item << 8 | tile << 4 | warp (bit 3
+ *       set when the tile is absent: S/128 odd). Records of a CTA that ran out
+ *       of items stay zero. clock64 values compare only within one CTA.
+ */
+xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                            int P, float scale, void *trace, size_t trace_bytes, void *stream);
+
+/* Grid size, items per CTA and trace bytes of xs_attn_a2a_trace for these
+ * shapes on the current device. */
+xs_status xs_attn_trace_layout(int B, int S, int H, int D, int P, int *ctas, int *items_per_cta, size_t *bytes);
+
 /* Human-readable description of the last non-OK status returned on this host
  * thread (empty string if none). The pointer stays valid until the next call
  * on this thread. */

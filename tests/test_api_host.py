@@ -19,9 +19,13 @@ def xs():
 
 
 def _declared_symbols():
-    src = open(os.path.join(ROOT, "include", "xs.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(xs_[a-z0-9_]+)\s*\(", src)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(xs_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_and_binding_agree(xs):
