@@ -84,13 +84,13 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-// Shape rules shared by every call. `attn` adds the multiple-of-128 rule.
+// Shape rules shared by every call.
 xs_status check_shape(int B, int S, int H, int D, int P, bool attn, size_t *bytes) {
+    (void)attn;
     if (B < 0 || S < 0) return fail(XS_ERR_SHAPE, "B and S must be >= 0 (got B=%d S=%d)", B, S);
     if (H < 1 || P < 1) return fail(XS_ERR_SHAPE, "H and P must be >= 1 (got H=%d P=%d)", H, P);
     if (H % P) return fail(XS_ERR_SHAPE, "H=%d is not a multiple of P=%d", H, P);
     if (S % P) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of P=%d", S, P);
-    if (attn && S % 128) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of 128", S);
     if (D != 64 && D != 128) return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64 or 128)", D);
     const unsigned long long rows = (unsigned long long)B * S * H;
     if (rows >= (1ull << 31)) return fail(XS_ERR_SHAPE, "B*S*H=%llu rows exceeds 2^31-1", rows);
@@ -182,9 +182,10 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
-    if (!std::isfinite(scale)) return fail(XS_ERR_SHAPE, "scale must be finite");
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(XS_ERR_SHAPE, "scale must be positive and finite");
     if (trace) {
         if (D != 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing is built for D=128 only (got D=%d)", D);
+        if (S % 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing needs S a multiple of 128 (got S=%d)", S);
         if (misaligned(trace)) return fail(XS_ERR_ALIGN, "trace must be 16-byte aligned");
     }
     if (layout == 1) {
@@ -234,9 +235,10 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     p.P = P;
     p.Hl = H / P;
     p.Sl = S / P;
-    p.n_qt = S / 128;
+    p.n_qt = (S + 127) / 128;
     p.n_pairs = (p.n_qt + 1) / 2;
-    p.n_kv = S / 128;
+    p.n_kv = (S + 127) / 128;
+    p.kv_tail = S - (p.n_kv - 1) * 128;
     const long long items = (long long)P * B * p.Hl * p.n_pairs;
     if (items >= (1ll << 31)) return fail(XS_ERR_SHAPE, "too many work items (%lld)", items);
     p.n_items = (int)items;
@@ -330,9 +332,9 @@ xs_status xs_attn_trace_layout(int B, int S, int H, int D, int P, int *ctas, int
     DeviceInfo info;
     if ((st = current_device(&dev, &info))) return st;
     xs::AttnParams p;
-    p.n_qt = S / 128;
+    p.n_qt = (S + 127) / 128;
     p.n_pairs = (p.n_qt + 1) / 2;
-    p.n_kv = S / 128;
+    p.n_kv = (S + 127) / 128;
     p.n_items = P * B * (H / P) * p.n_pairs;
     const int grid = xs::attn_schedule(p, info.num_sms, false);
     *ctas = grid;
@@ -353,8 +355,9 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
     int dev;
     DeviceInfo info;
     if ((st = current_device(&dev, &info))) return st;
-    const long long n_items = (long long)P * B * (H / P) * ((S / 128 + 1) / 2);
-    *bytes = xs::attn_workspace_bytes((int)n_items, S / 128, D, info.num_sms);
+    const int n_qt = (S + 127) / 128;
+    const long long n_items = (long long)P * B * (H / P) * ((n_qt + 1) / 2);
+    *bytes = xs::attn_workspace_bytes((int)n_items, n_qt, D, info.num_sms);
     return XS_OK;
 }
 

@@ -217,8 +217,9 @@ __device__ __forceinline__ float4 ld_cg4(const float4 *ptr) {
 }
 
 // Element offset of the first element of output row (rb, hl, token s).
-template <int D, int EPI>
+template <int D, int EPI, bool RAG>
 __device__ __forceinline__ int64_t out_row_offset(const AttnParams &p, int rb, int hl, int s) {
+    if (RAG && s >= p.S) return -1;  // a row of a partial last tile that does not exist
     if (EPI == 0) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
     const int b = rb % p.B, r = rb / p.B;
     const int h = r * p.Hl + hl;
@@ -244,7 +245,8 @@ __device__ __forceinline__ void stage_chunk(uint32_t stage, int lane, int c, uin
     const uint32_t a = stage + lane * 128 + ((c ^ (lane & 7)) << 4);
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1), "r"(x2), "r"(x3) : "memory");
 }
-__device__ __forceinline__ void flush_block(uint16_t *out, uint32_t stage, int lane, int64_t dst, int db) {
+template <bool GUARD>
+__device__ __forceinline__ void flush_rows(uint16_t *out, uint32_t stage, int lane, int64_t dst, int db) {
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -255,9 +257,27 @@ __device__ __forceinline__ void flush_block(uint16_t *out, uint32_t stage, int l
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y0), "=r"(y1), "=r"(y2), "=r"(y3) : "r"(a) : "memory");
         const int64_t d = __shfl_sync(0xffffffffu, dst, rr);
         uint16_t *gp = out + d + db * 64 + c * 8;
-        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gp), "r"(y0), "r"(y1), "r"(y2), "r"(y3) : "memory");
+        if (GUARD) {
+            // rows past S (d < 0) are not stored; the predicate stays inside the asm
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ge.s64 p, %5, 0;\n @p st.global.v4.b32 [%0], {%1, %2, %3, %4};\n}" ::"l"(gp),
+                "r"(y0), "r"(y1), "r"(y2), "r"(y3), "l"(d)
+                : "memory");
+        } else {
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gp), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+                         : "memory");
+        }
     }
     __syncwarp();
+}
+// Stores the warp's 32 staged rows. With RAG (S not a multiple of 128) a row
+// whose destination is -1 (past S in a partial last tile) is skipped.
+template <bool RAG>
+__device__ __forceinline__ void flush_block(uint16_t *out, uint32_t stage, int lane, int64_t dst, int db) {
+    if (RAG && __any_sync(0xffffffffu, dst < 0))
+        flush_rows<true>(out, stage, lane, dst, db);
+    else
+        flush_rows<false>(out, stage, lane, dst, db);
 }
 
 // ------------------------------------------------------------ split items
@@ -280,7 +300,7 @@ __device__ __forceinline__ const float *piece_record(const AttnParams &p, int c,
 // otherwise every piece, this CTA's included, comes from the workspace. Both
 // read the same bits, so the result does not depend on which piece merges.
 // CH columns (32 or 64) are gathered per round.
-template <int D, int CH>
+template <int D, int CH, bool RAG>
 __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, int lane, uint32_t stage, int c_first,
                                            int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
                                            uint32_t tO, int64_t dst, bool valid) {
@@ -342,7 +362,7 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
                             pack_bf16x2(acc[8 * c + 2] * inv_L, acc[8 * c + 3] * inv_L),
                             pack_bf16x2(acc[8 * c + 4] * inv_L, acc[8 * c + 5] * inv_L),
                             pack_bf16x2(acc[8 * c + 6] * inv_L, acc[8 * c + 7] * inv_L));
-            if ((col0 + CH) % 64 == 0) flush_block(p.out, stage, lane, dst, col0 / 64);
+            if ((col0 + CH) % 64 == 0) flush_block<RAG>(p.out, stage, lane, dst, col0 / 64);
         }
     }
 }
@@ -352,7 +372,7 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
 // TMEM) and return 0, or publish this piece's rows (unnormalised O, row max,
 // row sum) to the workspace and return 1: the caller must then count the
 // arrival with arrive_piece. `release` runs once the rows are out of TMEM.
-template <int D, int CH, typename Release>
+template <int D, int CH, bool RAG, typename Release>
 __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
                                                  uint32_t stage, int c_first, int c_last, uint32_t ua, float m, float l,
                                                  uint32_t tO, int64_t dst, bool valid, Release release) {
@@ -368,7 +388,7 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
     others = __shfl_sync(0xffffffffu, others, 0);
     if (others) {
         __threadfence();
-        merge_rows<D, CH>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst, valid);
+        merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst, valid);
         release();
         return 0;
     }
@@ -392,7 +412,7 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
 
 // Counts this piece's arrival for tile t (after its rows were published and
 // fenced); the last arrival merges from the workspace.
-template <int D, int CH>
+template <int D, int CH, bool RAG>
 __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
                                              uint32_t stage, int c_first, int c_last, uint32_t ua, int64_t dst,
                                              bool valid) {
@@ -405,7 +425,7 @@ __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, 
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
-    merge_rows<D, CH>(p, t, row, lane, stage, c_first, c_last, ua, false, 0.f, 0.f, 0u, dst, valid);
+    merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, false, 0.f, 0.f, 0u, dst, valid);
 }
 
 
@@ -447,7 +467,7 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD, int TRACE>
+template <int D, int EPI, int LD, int TRACE, bool RAG>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
@@ -676,6 +696,13 @@ __global__ void __launch_bounds__(512, 1)
                 // this thread's row of S: columns 0-63 in sa, 64-127 in sb
                 uint32_t sa[64], sb[64];
 #define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
+                if (RAG && g.j0 + j == p.n_kv - 1) {
+                    // keys past S (zero-filled rows of the last K/V tile) take no
+                    // weight: their scores become -inf in tensor memory
+#pragma unroll 1
+                    for (int c = p.kv_tail; c < 128; ++c) tmem_st1(tS + (uint32_t)c, f2u(-INFINITY));
+                    tmem_st_wait();
+                }
                 tmem_ld64(tS, sa);
                 tmem_ld64(tS + 64, sb);
                 float mx0 = fmaxf(u2f(sa[0]), u2f(sa[1])), mx1 = fmaxf(u2f(sa[2]), u2f(sa[3]));
@@ -766,14 +793,14 @@ __global__ void __launch_bounds__(512, 1)
                 const int c_first = sk_cta_of(ua, p), c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
-                const int64_t dst = out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row);
+                const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row);
                 const uint32_t stage = sQ + t * C::kTile + (warp & 3) * C::kStageWarp;
-                const uint32_t pend = finish_piece<D, 64>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
+                const uint32_t pend = finish_piece<D, 64, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
                                                           l, tO, dst, valid, [] {});
                 if (pend) {
                     __threadfence();
                     __syncwarp();
-                    arrive_piece<D, 64>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst, valid);
+                    arrive_piece<D, 64, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst, valid);
                 }
                 continue;
             }
@@ -818,7 +845,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
-                const int64_t dst = out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row);
+                const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row);
                 const uint32_t tO = tmem + lane_base + C::colO(t);
                 auto release_o = [&]() {  // O_t fully read: the next item may overwrite it
                     tc_fence_before();
@@ -826,7 +853,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
                 };
                 if (g.split) {
-                    pending |= finish_piece<D, 32>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO, dst,
+                    pending |= finish_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO, dst,
                                                    valid, release_o)
                                << t;
                     continue;
@@ -850,7 +877,7 @@ __global__ void __launch_bounds__(512, 1)
                                     pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
                     if (TRACE && db == 0) t_store = clock64_now();
-                    flush_block(p.out, stage, lane, dst, db);
+                    flush_block<RAG>(p.out, stage, lane, dst, db);
                 }
                 if (TRACE && lane == 0) {
                     const unsigned long long t_end = clock64_now();
@@ -870,8 +897,8 @@ __global__ void __launch_bounds__(512, 1)
             for (int t = 0; t < 2; ++t) {
                 if (!(pending & (1u << t))) continue;
                 const int qt = 2 * w.pair + t;
-                arrive_piece<D, 32>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
-                                    out_row_offset<D, EPI>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
+                arrive_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
+                                         out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
             }
         }
     }
@@ -924,14 +951,23 @@ size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     return rec + cnt;
 }
 
-template <int D, int EPI, int LD, int TRACE = 0>
-static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
-                            cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE>;
+template <int D, int EPI, int LD, int TRACE, bool RAG>
+static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
+                              cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
     return cudaGetLastError();
+}
+
+// The ragged instances (S not a multiple of 128) carry the key mask and the
+// row guard; the others compile without them.
+template <int D, int EPI, int LD>
+static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
+                            cudaStream_t stream) {
+    return p.kv_tail < 128 ? launch_one<D, EPI, LD, 0, true>(maps, p, grid, stream)
+                           : launch_one<D, EPI, LD, 0, false>(maps, p, grid, stream);
 }
 
 cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
@@ -943,7 +979,7 @@ cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const A
 
 cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                     cudaStream_t stream) {
-    if (D == 128) return launch_t<128, 1, 0, 1>(maps, p, grid, stream);
+    if (D == 128 && p.kv_tail == 128) return launch_one<128, 1, 0, 1, false>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -10,7 +10,8 @@ namespace xs {
 
 // Work decomposition of one attention call. A work item is a pair of
 // consecutive 128-row query tiles of one (rank, batch, local head); the second
-// tile of the last pair is absent when S/128 is odd. A unit is one item and
+// tile of the last pair is absent when ceil(S/128) is odd, and the last tile
+// is partial when S is not a multiple of 128. A unit is one item and
 // one 128-row K/V tile.
 //
 // Schedule: CTA c first takes whole items c, c + G, ..., c + (n_dp - 1) G
@@ -21,9 +22,10 @@ namespace xs {
 struct AttnParams {
     int B, S, H, P, Hl, Sl;
     int ld_rows;  // sequence-partitioned inputs: token rows per TMA box (gcd(Sl, 128))
-    int n_qt;     // 128-row query tiles per head  (S / 128)
+    int n_qt;     // 128-row query tiles per head  (ceil(S / 128))
     int n_pairs;  // work items per head           (ceil(n_qt / 2))
-    int n_kv;     // 128-row K/V tiles per head    (S / 128)
+    int n_kv;     // 128-row K/V tiles per head    (ceil(S / 128))
+    int kv_tail;  // keys in the last K/V tile (128 unless S is ragged); later columns are masked
     int n_items;  // P * B * Hl * n_pairs
     float scale_log2;  // scale * log2(e): softmax runs in base 2
     uint16_t *out;

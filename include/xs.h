@@ -40,8 +40,11 @@
  *     non-zero xs_status, enqueues nothing and leaves `out` untouched;
  *     xs_last_error() then describes it.
  *   - Shapes: B >= 0, S >= 0 (B == 0 or S == 0 is a valid empty call that
- *     enqueues nothing), H >= 1, P >= 1, H % P == 0, S % P == 0, S % 128 == 0,
- *     D in {64, 128}, scale finite. Every tensor must stay below 2^40 bytes.
+ *     enqueues nothing), H >= 1, P >= 1, H % P == 0, S % P == 0, D in {64, 128},
+ *     scale positive and finite. Every tensor must stay below 2^40 bytes. S need
+ *     not be a multiple of 128: the last query tile is then partial (rows past
+ *     S are neither computed into nor stored) and the keys past S in the last
+ *     K/V tile are masked out of the softmax.
  *   - `out` must not overlap q, k or v (XS_ERR_ALIAS).
  *   - The GPU must be compute capability 10.3 (sm_103); otherwise
  *     XS_ERR_UNSUPPORTED.
@@ -76,7 +79,7 @@ typedef enum {
  * section 4.3, Figure 7).
  *   q, k, v : head-partitioned [P][B][S][Hl][D] bf16, read only.
  *   out     : sequence-partitioned [P][B][Sl][H][D] bf16, fully overwritten.
- *   scale   : multiplies Q K^T before the softmax (usually 1/sqrt(D)).
+ *   scale   : multiplies Q K^T before the softmax (usually 1/sqrt(D)); > 0.
  * Each finished 128-row output tile of head (r, b, hl) is written straight into
  * the slices of the ranks that own its tokens. Bit-identical to
  * xs_a2a_permute(xs_attn(q, k, v)) for the same arguments.
@@ -99,8 +102,7 @@ xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B,
  *   in  : head-partitioned [P][B][S][Hl][D], 16-bit elements (any payload).
  *   out : sequence-partitioned [P][B][Sl][H][D], fully overwritten.
  * A pure copy: out is bit-for-bit a permutation of in. Same shape rules as the
- * attention calls except that scale does not apply and S need only satisfy
- * S % P == 0 (no multiple-of-128 rule). in and out must not overlap.
+ * attention calls except that scale does not apply. in and out must not overlap.
  */
 xs_status xs_a2a_permute(const void *in, void *out, int B, int S, int H, int D, int P, void *stream);
 
@@ -197,7 +199,7 @@ xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void 
  *       uint64: clock64 when the tile's O and row sums were ready, clock64 just
  *       before its first global store, clock64 after its last store was issued,
  *       %globaltimer (ns) when ready, and item << 8 | tile << 4 | warp (bit 3
- *       set when the tile is absent: S/128 odd). Records of a CTA that ran out
+ *       set when the tile is absent: ceil(S/128) odd). Records of a CTA that ran out
  *       of items stay zero. clock64 values compare only within one CTA.
  */
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,

@@ -63,13 +63,15 @@ def test_attention_argument_checks(xs, fn_name):
     assert _attn(xs, fn, o=0) == xs.XS_ERR_NULL
     assert "non-NULL" in xs.last_error()
     assert _attn(xs, fn, H=6, P=4) == xs.XS_ERR_SHAPE          # H % P
-    assert _attn(xs, fn, S=130, P=2) == xs.XS_ERR_SHAPE        # S % 128
+    assert _attn(xs, fn, S=131, P=2) == xs.XS_ERR_SHAPE        # S % P
     assert _attn(xs, fn, S=384, P=5, H=10) == xs.XS_ERR_SHAPE  # S % P
     assert _attn(xs, fn, H=0) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, P=0) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, B=-1) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, scale=float("nan")) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, scale=float("inf")) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, scale=0.0) == xs.XS_ERR_SHAPE
+    assert _attn(xs, fn, scale=-0.125) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, D=96) == xs.XS_ERR_UNSUPPORTED
     assert "D=96" in xs.last_error()
     assert _attn(xs, fn, q=Q + 8) == xs.XS_ERR_ALIGN
@@ -94,7 +96,7 @@ def test_workspace_argument_checks(xs):
     assert xs.attn_ws(0, K, V, O, 1, 256, 8, 64, 4, 0.1, W, 1 << 20, check=False) == xs.XS_ERR_NULL
     n = ctypes.c_size_t(7)
     assert xs.lib.xs_attn_workspace_size(1, 0, 8, 64, 4, ctypes.byref(n)) == xs.XS_OK and n.value == 0
-    assert xs.lib.xs_attn_workspace_size(1, 100, 8, 64, 4, ctypes.byref(n)) == xs.XS_ERR_SHAPE
+    assert xs.lib.xs_attn_workspace_size(1, 102, 8, 64, 4, ctypes.byref(n)) == xs.XS_ERR_SHAPE
     assert xs.lib.xs_attn_workspace_size(1, 256, 8, 64, 4, None) == xs.XS_ERR_NULL
 
 
@@ -105,7 +107,8 @@ def test_ulysses_argument_checks(xs):
         kw.get("scale", 0.125), ws, nb, check=False)
     assert f(q=0) == xs.XS_ERR_NULL
     assert f(H=6) == xs.XS_ERR_SHAPE
-    assert f(S=200) == xs.XS_ERR_SHAPE
+    assert f(S=202) == xs.XS_ERR_SHAPE                  # S % P
+    assert f(S=100) == xs.XS_ERR_UNSUPPORTED            # Sl = 25 is not a multiple of 8
     assert f(D=96) == xs.XS_ERR_UNSUPPORTED
     assert f(P=16, H=16) == xs.XS_ERR_UNSUPPORTED and "P=16" in xs.last_error()
     assert f(o=Q + 32) == xs.XS_ERR_ALIAS
