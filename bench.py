@@ -79,7 +79,7 @@ def workload_bytes(w) -> int:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("xs_attn.cu", "xs_ptx.cuh"):
+    for name in ("xs_attn_kernel.cuh", "xs_attn_d128.cu", "xs_ptx.cuh"):
         with open(os.path.join(ROOT, "comm_comp_fusion_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -285,6 +285,9 @@ def run_ours(args):
     # read as sequence-partitioned [P][B][Sl][H][D] (same size, same i.i.d.
     # values), against the serial composition: the pre-attention permute of each
     # operand, attention, and the post-attention permute.
+    uly_ok = xs.ulysses_attn(q, k, v, out_whole, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr,
+                             check=False) == xs.XS_OK
+    uly_why = None if uly_ok else xs.last_error()
     hq, hk, hv = (torch.empty_like(out) for _ in range(3))
     uly_out = torch.empty_like(out)
     ulysses = lambda: xs.ulysses_attn(q, k, v, uly_out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
@@ -319,8 +322,9 @@ def run_ours(args):
         fused_whole()
         attn()
         perm()
-        ulysses()
-        ulysses_serial()
+        if uly_ok:
+            ulysses()
+            ulysses_serial()
     torch.cuda.synchronize(dev)
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
 
@@ -346,7 +350,8 @@ def run_ours(args):
     # ---- Ulysses region: both All-to-Alls fused vs the post-only fused call
     # (the difference is the cost of reading from the sequence partition) and
     # vs the serial composition
-    t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps)
+    if uly_ok:
+        t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps)
     clocks = sampler.stop()
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
 
@@ -385,7 +390,18 @@ def run_ours(args):
     hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
     traffic = recorded_traffic(w["name"])
-    tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
+    if uly_ok:
+        tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
+        uly = {
+            "call": "xs_ulysses_attn (q, k, v, out sequence-partitioned; balanced schedule)",
+            "t_us": tu_us, "tflops": flops / (tu_us * 1e-6) / 1e12,
+            "pct_bf16_peak": 100.0 * flops / (tu_us * 1e-6) / 1e12 / peaks["bf16_tflops"],
+            "t_post_only_fused_us": tuf_us, "load_side_overhead_us": tu_us - tuf_us,
+            "t_serial_us": tus_us, "serial": "3 x xs_a2a_permute_inverse + xs_attn_ws + xs_a2a_permute",
+            "speedup_vs_serial": tus_us / tu_us, "t_inverse_permute_us": ti_us,
+        }
+    else:
+        uly = {"unavailable": uly_why}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -413,14 +429,7 @@ def run_ours(args):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic,
                      "algorithmic_flop_per_launch": flops, "algorithmic_min_bytes_per_launch": 4 * nbytes},
-        "ulysses": {
-            "call": "xs_ulysses_attn (q, k, v, out sequence-partitioned; balanced schedule)",
-            "t_us": tu_us, "tflops": flops / (tu_us * 1e-6) / 1e12,
-            "pct_bf16_peak": 100.0 * flops / (tu_us * 1e-6) / 1e12 / peaks["bf16_tflops"],
-            "t_post_only_fused_us": tuf_us, "load_side_overhead_us": tu_us - tuf_us,
-            "t_serial_us": tus_us, "serial": "3 x xs_a2a_permute_inverse + xs_attn_ws + xs_a2a_permute",
-            "speedup_vs_serial": tus_us / tu_us, "t_inverse_permute_us": ti_us,
-        },
+        "ulysses": uly,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
                 "ms_per_step": e2e_max / args.steps},
         "gpu_launches": gpu_launches,

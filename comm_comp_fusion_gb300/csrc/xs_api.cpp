@@ -91,7 +91,7 @@ xs_status check_shape(int B, int S, int H, int D, int P, bool attn, size_t *byte
     if (H < 1 || P < 1) return fail(XS_ERR_SHAPE, "H and P must be >= 1 (got H=%d P=%d)", H, P);
     if (H % P) return fail(XS_ERR_SHAPE, "H=%d is not a multiple of P=%d", H, P);
     if (S % P) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of P=%d", S, P);
-    if (D != 64 && D != 128) return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64 or 128)", D);
+    if (D != 64 && D != 96 && D != 128) return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64, 96 or 128)", D);
     const unsigned long long rows = (unsigned long long)B * S * H;
     if (rows >= (1ull << 31)) return fail(XS_ERR_SHAPE, "B*S*H=%llu rows exceeds 2^31-1", rows);
     *bytes = (size_t)rows * D * 2;
@@ -380,7 +380,11 @@ xs_status permute_call(const void *in, void *out, int B, int S, int H, int D, in
 
     xs::PermParams p;
     p.rows = (uint32_t)((unsigned long long)B * S * H);
+    p.cpr = (uint32_t)(D / 8);
     p.cpr_log2 = D == 128 ? 4u : 3u;
+    xs::fastdiv_magic(p.cpr, &p.mC, &p.sC);
+    if (D == 96 && (unsigned long long)p.rows * p.cpr >= (1ull << 31))
+        return fail(XS_ERR_SHAPE, "a D=96 permute handles at most 2^31 16-byte chunks (tensor below 32 GiB)");
     p.B = (uint32_t)B;
     p.S = (uint32_t)S;
     p.H = (uint32_t)H;

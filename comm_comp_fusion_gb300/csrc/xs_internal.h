@@ -77,6 +77,19 @@ cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const Att
 cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
                            cudaStream_t stream);
 
+// Per-head-dimension instances (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu).
+#define XS_DECLARE_ATTN_ENTRY(D)                                                                                  \
+    cudaError_t launch_attention_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
+                                      cudaStream_t stream);                                                       \
+    cudaError_t launch_ulysses_d##D(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,             \
+                                    cudaStream_t stream);                                                         \
+    cudaError_t read_error_word_d##D(unsigned int *value, bool clear);
+XS_DECLARE_ATTN_ENTRY(64)
+XS_DECLARE_ATTN_ENTRY(96)
+XS_DECLARE_ATTN_ENTRY(128)
+cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                                         cudaStream_t stream);
+
 // Sets the calling thread's xs_last_error() text; returns `status`.
 int report_error(int status, const char *message);
 
@@ -86,7 +99,9 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t strea
 
 struct PermParams {
     uint32_t rows;       // B * S * H rows of D elements
-    uint32_t cpr_log2;   // log2(16-byte chunks per row)
+    uint32_t cpr;        // 16-byte chunks per row (D / 8)
+    uint32_t cpr_log2;   // log2(cpr) when cpr is a power of two
+    uint32_t mC, sC;     // magic numbers for division by cpr otherwise
     uint32_t B, S, H, Hl, Sl;
     // magic numbers for division by H, Sl, B, Hl and S (round-up method)
     uint32_t mH, sH, mSl, sSl, mB, sB, mHl, sHl, mS, sS;

@@ -66,40 +66,44 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *ptr) {
 constexpr int kPermThreads = 256;
 constexpr int kPermUnroll = 4;
 
-template <bool INV>
+// Source chunk of output chunk o: rows of 2^cpr_log2 chunks (POW2), or of
+// p.cpr chunks with o below 2^31 (D = 96: 12 chunks per row).
+template <bool INV, bool POW2>
+__device__ __forceinline__ uint64_t src_chunk(uint64_t o, const PermParams &p) {
+    if (POW2) {
+        const uint32_t orow = (uint32_t)(o >> p.cpr_log2);
+        return ((uint64_t)src_chunk_row<INV>(orow, p) << p.cpr_log2) | (o & ((1u << p.cpr_log2) - 1u));
+    }
+    const uint32_t orow = fdiv((uint32_t)o, p.mC, p.sC);
+    return (uint64_t)src_chunk_row<INV>(orow, p) * p.cpr + ((uint32_t)o - orow * p.cpr);
+}
+
+template <bool INV, bool POW2>
 __global__ void __launch_bounds__(kPermThreads) a2a_permute_kernel(const uint4 *__restrict__ in,
                                                                    uint4 *__restrict__ out, const PermParams p) {
-    const uint64_t total = (uint64_t)p.rows << p.cpr_log2;
+    const uint64_t total = (uint64_t)p.rows * p.cpr;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    const uint32_t cmask = (1u << p.cpr_log2) - 1u;
     uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; i + (kPermUnroll - 1) * stride < total; i += kPermUnroll * stride) {
         uint4 v[kPermUnroll];
 #pragma unroll
-        for (int u = 0; u < kPermUnroll; ++u) {
-            const uint64_t o = i + u * stride;
-            const uint32_t orow = (uint32_t)(o >> p.cpr_log2);
-            const uint64_t src = ((uint64_t)src_chunk_row<INV>(orow, p) << p.cpr_log2) | (o & cmask);
-            v[u] = ld_stream(in + src);
-        }
+        for (int u = 0; u < kPermUnroll; ++u) v[u] = ld_stream(in + src_chunk<INV, POW2>(i + u * stride, p));
 #pragma unroll
         for (int u = 0; u < kPermUnroll; ++u) out[i + u * stride] = v[u];
     }
-    for (; i < total; i += stride) {
-        const uint32_t orow = (uint32_t)(i >> p.cpr_log2);
-        const uint64_t src = ((uint64_t)src_chunk_row<INV>(orow, p) << p.cpr_log2) | (i & cmask);
-        out[i] = ld_stream(in + src);
-    }
+    for (; i < total; i += stride) out[i] = ld_stream(in + src_chunk<INV, POW2>(i, p));
 }
 
 cudaError_t launch_permute(const void *in, void *out, const PermParams &p, bool inverse, int num_sms,
                            cudaStream_t stream) {
-    const uint64_t total = (uint64_t)p.rows << p.cpr_log2;
+    const uint64_t total = (uint64_t)p.rows * p.cpr;
     uint64_t blocks = (total + kPermThreads - 1) / kPermThreads;
     const uint64_t cap = (uint64_t)num_sms * (2048 / kPermThreads);  // one full wave of resident threads
     if (blocks > cap) blocks = cap;
     if (blocks == 0) return cudaSuccess;
-    auto kern = inverse ? a2a_permute_kernel<true> : a2a_permute_kernel<false>;
+    const bool pow2 = (p.cpr & (p.cpr - 1u)) == 0u;
+    auto kern = inverse ? (pow2 ? a2a_permute_kernel<true, true> : a2a_permute_kernel<true, false>)
+                        : (pow2 ? a2a_permute_kernel<false, true> : a2a_permute_kernel<false, false>);
     kern<<<(unsigned)blocks, kPermThreads, 0, stream>>>(static_cast<const uint4 *>(in), static_cast<uint4 *>(out), p);
     return cudaGetLastError();
 }

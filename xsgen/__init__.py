@@ -72,7 +72,7 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return (u >> 16).astype(np.uint16)
 
 
-# The five synthetic workloads: (B, S, H, D, P, sigma_qk, sigma_v, scale, name).
+# The synthetic workloads: (B, S, H, D, P, sigma_qk, sigma_v, scale, name).
 WORKLOADS = [
     dict(B=1, S=256, H=8, D=64, P=4, sigma_qk=1.0, sigma_v=1.0, scale=1.0 / 8.0,
          name="small: B=1 S=256 H=8 D=64 P=4"),
@@ -84,6 +84,12 @@ WORKLOADS = [
          name="long video DiT: B=1 S=32768 H=16 D=128 P=8"),
     dict(B=2, S=16384, H=40, D=128, P=4, sigma_qk=2.0 ** 0.5, sigma_v=1.0, scale=128 ** -0.5,
          name="peaked: B=2 S=16384 H=40 D=128 P=4, Q,K ~ N(0,2)"),
+    # shape variants (measured, not the headline): a sequence length that is
+    # not a multiple of the 128-row tile, and head dimension 96
+    dict(B=1, S=4032, H=24, D=128, P=8, sigma_qk=1.0, sigma_v=1.0, scale=128 ** -0.5,
+         name="ragged DiT: B=1 S=4032 H=24 D=128 P=8"),
+    dict(B=1, S=8192, H=32, D=96, P=8, sigma_qk=1.0, sigma_v=1.0, scale=96 ** -0.5,
+         name="D=96: B=1 S=8192 H=32 D=96 P=8"),
 ]
 
 
