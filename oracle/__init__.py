@@ -11,7 +11,10 @@ Passages followed (X-Stage paper, arXiv 2607.23264v1):
   * section 4.3, Figure 5 (d-e) -- the Ulysses post-attention All-to-All that
     turns the head partition back into the sequence partition;
   * section 5.3 -- "Serial" = attention followed by that All-to-All, which is
-    exactly what ``attention_a2a`` returns.
+    exactly what ``attention_a2a`` returns;
+  * section 4.3's contrast with "the causal attention used by typical
+    autoregressive LLMs" -- ``causal=True`` restricts query token i to keys
+    0..i (the standard autoregressive mask; the pages do not write it out).
 
 Every function here is pinned by ``tests/test_oracle.py`` against brute force,
 closed forms, invariants and hand-derived fixtures in ``tests/golden/``.
@@ -52,6 +55,13 @@ def _load():
         lib.xs_oracle_attention_rows.restype = ctypes.c_int
         lib.xs_oracle_attention_a2a.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ctypes.c_int]
         lib.xs_oracle_attention_a2a.restype = ctypes.c_int
+        ci = ctypes.c_int
+        lib.xs_oracle_attention_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
+        lib.xs_oracle_attention_ex.restype = ci
+        lib.xs_oracle_attention_rows_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, vp, i64, vp, ci]
+        lib.xs_oracle_attention_rows_ex.restype = ci
+        lib.xs_oracle_attention_a2a_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
+        lib.xs_oracle_attention_a2a_ex.restype = ci
         lib.xs_oracle_a2a.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
         lib.xs_oracle_a2a.restype = ctypes.c_int
         lib.xs_oracle_a2a_inverse.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
@@ -83,32 +93,34 @@ def default_threads() -> int:
     return _load().xs_oracle_default_threads()
 
 
-def attention(q, k, v, B, S, H, D, P, scale, nthreads=0, return_threads=False):
-    """Head-partitioned fp64 attention output, shape [P][B][S][H/P][D]."""
+def attention(q, k, v, B, S, H, D, P, scale, nthreads=0, return_threads=False, causal=False):
+    """Head-partitioned fp64 attention output, shape [P][B][S][H/P][D]; with
+    causal=True query token i sees keys 0..i only."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     out = np.empty((P, B, S, H // P, D), dtype=np.float64)
-    used = _check(_load().xs_oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                              out.ctypes.data, B, S, H, D, P, float(scale), nthreads))
+    used = _check(_load().xs_oracle_attention_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                 out.ctypes.data, B, S, H, D, P, float(scale), int(causal),
+                                                 nthreads))
     return (out, used) if return_threads else out
 
 
-def attention_rows(q, k, v, B, S, H, D, P, scale, rows, nthreads=0, return_threads=False):
+def attention_rows(q, k, v, B, S, H, D, P, scale, rows, nthreads=0, return_threads=False, causal=False):
     """fp64 attention for selected head-partitioned rows ((r*B+b)*S+s)*Hl+hl -> [n][D]."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     out = np.empty((rows.size, D), dtype=np.float64)
-    used = _check(_load().xs_oracle_attention_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                                   B, S, H, D, P, float(scale), rows.ctypes.data,
-                                                   rows.size, out.ctypes.data, nthreads))
+    used = _check(_load().xs_oracle_attention_rows_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                      B, S, H, D, P, float(scale), int(causal), rows.ctypes.data,
+                                                      rows.size, out.ctypes.data, nthreads))
     return (out, used) if return_threads else out
 
 
-def attention_a2a(q, k, v, B, S, H, D, P, scale, nthreads=0):
+def attention_a2a(q, k, v, B, S, H, D, P, scale, nthreads=0, causal=False):
     """Attention then the All-to-All, fp64, shape [P][B][S/P][H][D]."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     out = np.empty((P, B, S // P, H, D), dtype=np.float64)
-    _check(_load().xs_oracle_attention_a2a(q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                           out.ctypes.data, B, S, H, D, P, float(scale), nthreads))
+    _check(_load().xs_oracle_attention_a2a_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                              out.ctypes.data, B, S, H, D, P, float(scale), int(causal), nthreads))
     return out
 
 

@@ -18,6 +18,11 @@
  *    exponentials and sums). The online rescaling recurrence that FlashAttention
  *    uses reaches the same value up to rounding; the oracle does not use it.
  *
+ *  - Causal attention (section 4.3 contrasts the DiT setting with "the causal
+ *    attention used by typical autoregressive LLMs"; the pages do not write it
+ *    out). Reading taken: query token i of a head sees key tokens j <= i of the
+ *    same sequence, so every sum above runs over j = 0..i instead of 0..S-1.
+ *
  *  - Ulysses post-attention All-to-All (section 4.3, Figure 5 d-e): attention
  *    runs head-partitioned (rank r holds heads r*Hl .. r*Hl+Hl-1 for all S
  *    tokens); the All-to-All restores the sequence partition (rank r' holds
@@ -132,6 +137,7 @@ typedef struct {
     const uint16_t *q, *k, *v;
     int64_t B, S, H, D, P;
     double scale;
+    int causal;        /* 1: query token i sees keys 0..i only */
     /* row list: head-partitioned row ids ((r*B+b)*S+s)*Hl+hl; NULL = all rows */
     const int64_t *rows;
     int64_t nrows;
@@ -152,26 +158,29 @@ static void attend_row(const attn_job_t *j, int64_t row, double *p, double *qi, 
 
     for (int64_t d = 0; d < D; ++d) qi[d] = bf16_to_double(j->q[head_base + s_i * row_stride + d]);
 
+    /* the keys this query sees: all S, or 0..s_i when causal */
+    const int64_t t0 = 0, t1 = j->causal ? s_i + 1 : S;
+
     /* scores s_j = scale * <q_i, k_j> */
-    for (int64_t t = 0; t < S; ++t) {
+    for (int64_t t = t0; t < t1; ++t) {
         const uint16_t *kt = j->k + head_base + t * row_stride;
         double acc = 0.0;
         for (int64_t d = 0; d < D; ++d) acc += qi[d] * bf16_to_double(kt[d]);
         p[t] = j->scale * acc;
     }
     /* m = max_j s_j */
-    double m = p[0];
-    for (int64_t t = 1; t < S; ++t)
+    double m = p[t0];
+    for (int64_t t = t0 + 1; t < t1; ++t)
         if (p[t] > m) m = p[t];
     /* p_j = exp(s_j - m), l = sum_j p_j */
     double l = 0.0;
-    for (int64_t t = 0; t < S; ++t) {
+    for (int64_t t = t0; t < t1; ++t) {
         p[t] = exp(p[t] - m);
         l += p[t];
     }
     /* o = sum_j p_j v_j / l ; for every d the sum runs over j in ascending order */
     for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
-    for (int64_t t = 0; t < S; ++t) {
+    for (int64_t t = t0; t < t1; ++t) {
         const uint16_t *vt = j->v + head_base + t * row_stride;
         for (int64_t d = 0; d < D; ++d) o[d] += p[t] * bf16_to_double(vt[d]);
     }
@@ -229,48 +238,66 @@ static int run_attention(attn_job_t base, int64_t total, int nthreads) {
 }
 
 /* Attention for every (r, b, hl) head; o is head-partitioned [P][B][S][Hl][D].
- * Returns the number of threads used (> 0), or a negative error. */
-int xs_oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *o, int64_t B,
-                        int64_t S, int64_t H, int64_t D, int64_t P, double scale, int nthreads) {
+ * causal = 1 restricts query i to keys 0..i. Returns the number of threads
+ * used (> 0), or a negative error. */
+int xs_oracle_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *o, int64_t B,
+                           int64_t S, int64_t H, int64_t D, int64_t P, double scale, int causal, int nthreads) {
     if (check_shape(B, S, H, D, P)) return XSO_EINVAL;
     int64_t total = P * B * S * (H / P);
     if (total == 0) return 1;
     if (!q || !k || !v || !o) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, B, S, H, D, P, scale, 0, 0, o, 0, 0, 0};
+    attn_job_t base = {q, k, v, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
     return run_attention(base, total, nthreads);
 }
 
+int xs_oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *o, int64_t B,
+                        int64_t S, int64_t H, int64_t D, int64_t P, double scale, int nthreads) {
+    return xs_oracle_attention_ex(q, k, v, o, B, S, H, D, P, scale, 0, nthreads);
+}
+
 /* Attention for a list of head-partitioned row ids; o_rows is [nrows][D]. */
-int xs_oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B,
-                             int64_t S, int64_t H, int64_t D, int64_t P, double scale,
-                             const int64_t *rows, int64_t nrows, double *o_rows, int nthreads) {
+int xs_oracle_attention_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B,
+                                int64_t S, int64_t H, int64_t D, int64_t P, double scale, int causal,
+                                const int64_t *rows, int64_t nrows, double *o_rows, int nthreads) {
     if (check_shape(B, S, H, D, P) || nrows < 0) return XSO_EINVAL;
     if (nrows == 0) return 1;
     if (!q || !k || !v || !rows || !o_rows) return XSO_EINVAL;
     int64_t total_rows = P * B * S * (H / P);
     for (int64_t i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total_rows) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, B, S, H, D, P, scale, rows, nrows, o_rows, 0, 0, 0};
+    attn_job_t base = {q, k, v, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
     return run_attention(base, nrows, nthreads);
+}
+
+int xs_oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B,
+                             int64_t S, int64_t H, int64_t D, int64_t P, double scale,
+                             const int64_t *rows, int64_t nrows, double *o_rows, int nthreads) {
+    return xs_oracle_attention_rows_ex(q, k, v, B, S, H, D, P, scale, 0, rows, nrows, o_rows, nthreads);
 }
 
 /* Fused reference: attention followed by the All-to-All of its fp64 result.
  * out is sequence-partitioned [P][B][Sl][H][D] (doubles). */
-int xs_oracle_attention_a2a(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
-                            int64_t B, int64_t S, int64_t H, int64_t D, int64_t P, double scale,
-                            int nthreads) {
+int xs_oracle_attention_a2a_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
+                               int64_t B, int64_t S, int64_t H, int64_t D, int64_t P, double scale, int causal,
+                               int nthreads) {
     if (check_shape(B, S, H, D, P)) return XSO_EINVAL;
     int64_t n = P * B * S * (H / P) * D;
     if (n == 0) return 1;
     double *tmp = (double *)malloc(sizeof(double) * (size_t)n);
     if (!tmp) return XSO_ENOMEM;
-    int used = xs_oracle_attention(q, k, v, tmp, B, S, H, D, P, scale, nthreads);
+    int used = xs_oracle_attention_ex(q, k, v, tmp, B, S, H, D, P, scale, causal, nthreads);
     if (used > 0) {
         int e = xs_oracle_a2a(tmp, out, B, S, H, D, P, (int64_t)sizeof(double));
         if (e) used = e;
     }
     free(tmp);
     return used;
+}
+
+int xs_oracle_attention_a2a(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out,
+                            int64_t B, int64_t S, int64_t H, int64_t D, int64_t P, double scale,
+                            int nthreads) {
+    return xs_oracle_attention_a2a_ex(q, k, v, out, B, S, H, D, P, scale, 0, nthreads);
 }
 
 int xs_oracle_default_threads(void) { return resolve_threads(0); }

@@ -33,8 +33,9 @@ def _scale(s):
     return {"ln3": math.log(3.0), "ln2": math.log(2.0)}[s] if isinstance(s, str) else float(s)
 
 
-def _brute(q, k, v, B, S, H, D, P, scale, dps=40):
-    """exp(s_j) / sum_k exp(s_k) without max subtraction, in 40-digit arithmetic."""
+def _brute(q, k, v, B, S, H, D, P, scale, dps=40, causal=False):
+    """exp(s_j) / sum_k exp(s_k) without max subtraction, in 40-digit arithmetic;
+    with causal, query i sums over keys j <= i only."""
     mp = pytest.importorskip("mpmath")
     mp.mp.dps = dps
     qf, kf, vf = (xsgen.bf16_bits_to_f32(x).astype(np.float64) for x in (q, k, v))
@@ -45,12 +46,13 @@ def _brute(q, k, v, B, S, H, D, P, scale, dps=40):
         for b in range(B):
             for hl in range(Hl):
                 for i in range(S):
+                    keys = range(i + 1) if causal else range(S)
                     w = [mp.exp(sc * mp.fsum(mp.mpf(qf[r, b, i, hl, d]) * mp.mpf(kf[r, b, j, hl, d])
-                                            for d in range(D))) for j in range(S)]
+                                            for d in range(D))) for j in keys]
                     tot = mp.fsum(w)
                     for d in range(D):
-                        out[r, b, i, hl, d] = float(mp.fsum(w[j] * mp.mpf(vf[r, b, j, hl, d])
-                                                            for j in range(S)) / tot)
+                        out[r, b, i, hl, d] = float(mp.fsum(w[n] * mp.mpf(vf[r, b, j, hl, d])
+                                                            for n, j in enumerate(keys)) / tot)
     return out
 
 
@@ -115,6 +117,56 @@ def test_brute_force_large_logits():
     o = oracle.attention(q, k, v, B, S, H, D, P, scale)
     assert np.isfinite(o).all()
     np.testing.assert_allclose(o, _brute(q, k, v, B, S, H, D, P, scale, dps=60), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ causal pins
+# The causal reading: query token i sees keys 0..i of its own sequence.
+
+@pytest.mark.parametrize("case", TINY)
+def test_causal_brute_force_tiny(case):
+    B, S, H, D, P, scale, sigma = case
+    q, k, v = xsgen.random_inputs(91 + S * 10 + D, P, B, S, H, D, sigma, 1.0)
+    o = oracle.attention(q, k, v, B, S, H, D, P, scale, causal=True)
+    np.testing.assert_allclose(o, _brute(q, k, v, B, S, H, D, P, scale, causal=True), rtol=0, atol=1e-12)
+
+
+def test_causal_first_row_is_its_own_value():
+    """Token 0 sees only key 0: its output is v_0 exactly, for every head."""
+    B, S, H, D, P = 2, 10, 4, 8, 2
+    q, k, v = xsgen.random_inputs(12, P, B, S, H, D, 2.0, 1.0)
+    o = oracle.attention(q, k, v, B, S, H, D, P, 0.3, causal=True)
+    assert np.array_equal(o[:, :, 0], xsgen.bf16_bits_to_f32(v[:, :, 0]).astype(np.float64))
+
+
+def test_causal_last_row_sees_everything():
+    B, S, H, D, P = 1, 12, 4, 8, 2
+    q, k, v = xsgen.random_inputs(13, P, B, S, H, D)
+    c = oracle.attention(q, k, v, B, S, H, D, P, 0.3, causal=True)
+    f = oracle.attention(q, k, v, B, S, H, D, P, 0.3)
+    assert np.array_equal(c[:, :, S - 1], f[:, :, S - 1])
+    assert not np.allclose(c[:, :, : S - 1], f[:, :, : S - 1])
+
+
+def test_causal_row_is_full_attention_over_its_prefix():
+    """Row i of causal attention equals row i of full attention over tokens 0..i."""
+    B, S, H, D, P = 1, 10, 2, 4, 1
+    q, k, v = xsgen.random_inputs(14, P, B, S, H, D)
+    c = oracle.attention(q, k, v, B, S, H, D, P, 0.5, causal=True)
+    for i in (0, 3, 9):
+        pre = [np.ascontiguousarray(x[:, :, : i + 1]) for x in (q, k, v)]
+        f = oracle.attention(*pre, B, i + 1, H, D, P, 0.5)
+        np.testing.assert_allclose(c[:, :, i], f[:, :, i], rtol=0, atol=1e-15)
+
+
+def test_causal_rows_and_a2a_apis_agree():
+    B, S, H, D, P = 2, 8, 4, 4, 2
+    q, k, v = xsgen.random_inputs(15, P, B, S, H, D)
+    full = oracle.attention(q, k, v, B, S, H, D, P, 0.4, causal=True)
+    rows = np.array([0, 5, 17, P * B * S * (H // P) - 1])
+    np.testing.assert_array_equal(oracle.attention_rows(q, k, v, B, S, H, D, P, 0.4, rows, causal=True),
+                                  full.reshape(-1, D)[rows])
+    np.testing.assert_array_equal(oracle.attention_a2a(q, k, v, B, S, H, D, P, 0.4, causal=True),
+                                  oracle.a2a(full, B, S, H, D, P))
 
 
 # ------------------------------------------------------------------ invariants
@@ -261,6 +313,10 @@ _MUTANTS = {
     "token slot": ("int64_t sl = s - rd * Sl;", "int64_t sl = s % P;"),
     "head order": ("int64_t h = r * Hl + hl;", "int64_t h = hl * P + r;"),
     "rank of token": ("int64_t rd = s / Sl;", "int64_t rd = s % P;"),
+    "causal drops the diagonal": ("j->causal ? s_i + 1 : S", "j->causal ? s_i : S"),
+    "causal looks ahead": ("const int64_t t0 = 0, t1 = j->causal ? s_i + 1 : S;",
+                           "const int64_t t0 = j->causal ? s_i : 0, t1 = S;"),
+    "causal mask ignored": ("j->causal ? s_i + 1 : S", "S"),
 }
 
 
@@ -269,6 +325,8 @@ def _pins_pass(lib):
     vp, i64, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
     lib.xs_oracle_attention.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ctypes.c_int]
     lib.xs_oracle_a2a.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
+    lib.xs_oracle_attention_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ctypes.c_int,
+                                           ctypes.c_int]
 
     def attn(q, k, v, B, S, H, D, P, sc):
         o = np.empty((P, B, S, H // P, D))
@@ -276,7 +334,17 @@ def _pins_pass(lib):
                                 B, S, H, D, P, sc, 2)
         return o
 
+    def attn_causal(q, k, v, B, S, H, D, P, sc):
+        o = np.empty((P, B, S, H // P, D))
+        lib.xs_oracle_attention_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data,
+                                   B, S, H, D, P, sc, 1, 2)
+        return o
+
     ok = True
+    B, S, H, D, P, scale, sigma = TINY[3]
+    q, k, v = xsgen.random_inputs(91 + S * 10 + D, P, B, S, H, D, sigma, 1.0)
+    ok &= bool(np.allclose(attn_causal(q, k, v, B, S, H, D, P, scale),
+                           _brute(q, k, v, B, S, H, D, P, scale, causal=True), rtol=0, atol=1e-12))
     g = json.load(open(os.path.join(GOLDEN, "attn_closed_form.json")))
     for c in g["cases"]:
         o = attn(_bf16(c["q"]), _bf16(c["k"]), _bf16(c["v"]), c["B"], c["S"], c["H"], c["D"], c["P"],
