@@ -67,9 +67,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_flops(w) -> float:
-    """Algorithmic work of one call: QK^T and PV, 2 * S * S * D each per (b, h)."""
-    return 4.0 * w["B"] * w["H"] * w["S"] * w["S"] * w["D"]
+def workload_flops(w, causal: bool = False) -> float:
+    """Algorithmic work of one call: QK^T and PV, 2 * D per (query, key) pair each,
+    over S * S pairs per (b, h), or the S * (S + 1) / 2 pairs j <= i when causal."""
+    pairs = w["S"] * (w["S"] + 1) / 2.0 if causal else float(w["S"]) * w["S"]
+    return 4.0 * w["B"] * w["H"] * pairs * w["D"]
 
 
 def workload_bytes(w) -> int:
@@ -179,7 +181,7 @@ def barrier(world: int):
 
 # --------------------------------------------------------------- CPU oracle leg
 
-def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0):
+def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0, causal: bool = False):
     """Times the fp64 oracle on about `seconds` of sampled query rows of workload w.
     Returns (tflops, rows, wall_s, threads)."""
     import numpy as np
@@ -190,14 +192,16 @@ def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0):
     threads = oracle.default_threads()
     probe = rng.integers(0, total_rows, max(threads, 16))
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], probe)
+    oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], probe, causal=causal)
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(max(threads, min(total_rows, len(probe) * seconds / dt)))
     rows = rng.integers(0, total_rows, n)
     t0 = time.perf_counter()
-    _, used = oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], rows, return_threads=True)
+    _, used = oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], rows, return_threads=True, causal=causal)
     wall = time.perf_counter() - t0
-    flops = 4.0 * S * D * n
+    # a row of token s sees S keys, or s + 1 when causal: 4 * D flop per key
+    keys = (((rows // (H // P)) % S) + 1).sum() if causal else S * n
+    flops = 4.0 * D * float(keys)
     return flops / wall / 1e12, n, wall, used
 
 
@@ -211,22 +215,24 @@ def run_reference(args):
     # Each step is a bounded sample so that warm-up plus K steps stay within a few minutes.
     per_step = args.ref_step_seconds or max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
-        oracle_rows_rate(w, q, k, v, per_step / 4, seed=100 + i)
-    rates, rows_total, wall_total, threads = [], 0, 0.0, 0
+        oracle_rows_rate(w, q, k, v, per_step / 4, seed=100 + i, causal=args.causal)
+    flop_total, rows_total, wall_total, threads = 0.0, 0, 0.0, 0
     for i in range(args.steps):
-        r, n, wall, threads = oracle_rows_rate(w, q, k, v, per_step, seed=i)
-        rates.append(r)
+        r, n, wall, threads = oracle_rows_rate(w, q, k, v, per_step, seed=i, causal=args.causal)
+        flop_total += r * 1e12 * wall
         rows_total += n
         wall_total += wall
-    value = 4.0 * w["S"] * w["D"] * rows_total / wall_total / 1e12
+    value = flop_total / wall_total / 1e12
     sample = (f"{rows_total} query rows drawn uniformly from the {w['B'] * w['S'] * w['H']} rows of the workload "
-              f"over {args.steps} steps (~{per_step:.1f} s each); a row costs 4*S*D flop")
+              f"over {args.steps} steps (~{per_step:.1f} s each); a row costs 4*D flop per visible key"
+              + (" (causal)" if args.causal else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "S": w["S"], "H": w["H"], "D": w["D"], "P": w["P"],
-                   "parallelism": "replicas", "what": "fp64 CPU oracle (two-pass softmax attention per row)"},
+                   "parallelism": "replicas", "mask": "causal" if args.causal else "none",
+                   "what": "fp64 CPU oracle (two-pass softmax attention per row)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -256,7 +262,7 @@ def run_ours(args):
     w = xsgen.WORKLOADS[args.workload]
     B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
     nbytes = workload_bytes(w)
-    flops = workload_flops(w)
+    flops = workload_flops(w, args.causal)
     q_h, k_h, v_h = xsgen.workload_inputs(args.workload)
     as_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(dev)
     q, k, v = as_dev(q_h), as_dev(k_h), as_dev(v_h)
@@ -272,9 +278,14 @@ def run_ours(args):
 
     # The timed call is the balanced-schedule fused call (the library's fastest
     # fused path); the whole-item call is timed beside it for reference.
-    fused = lambda: xs.attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
-    fused_whole = lambda: xs.attn_a2a(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
-    attn = lambda: xs.attn_ws(q, k, v, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+    if args.causal:  # causal attention runs the whole-item schedule only
+        fused = lambda: xs.attn_causal_a2a(q, k, v, out, B, S, H, D, P, scale, stream=sptr)
+        fused_whole = lambda: xs.attn_causal_a2a(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
+        attn = lambda: xs.attn_causal(q, k, v, head, B, S, H, D, P, scale, stream=sptr)
+    else:
+        fused = lambda: xs.attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+        fused_whole = lambda: xs.attn_a2a(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
+        attn = lambda: xs.attn_ws(q, k, v, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
     perm = lambda: xs.a2a_permute(head, serial, B, S, H, D, P, stream=sptr)
 
     def serial_fn():
@@ -285,9 +296,12 @@ def run_ours(args):
     # read as sequence-partitioned [P][B][Sl][H][D] (same size, same i.i.d.
     # values), against the serial composition: the pre-attention permute of each
     # operand, attention, and the post-attention permute.
-    uly_ok = xs.ulysses_attn(q, k, v, out_whole, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr,
-                             check=False) == xs.XS_OK
-    uly_why = None if uly_ok else xs.last_error()
+    if args.causal:
+        uly_ok, uly_why = False, "the sequence-partitioned-load call is non-causal only"
+    else:
+        uly_ok = xs.ulysses_attn(q, k, v, out_whole, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr,
+                                 check=False) == xs.XS_OK
+        uly_why = None if uly_ok else xs.last_error()
     hq, hk, hv = (torch.empty_like(out) for _ in range(3))
     uly_out = torch.empty_like(out)
     ulysses = lambda: xs.ulysses_attn(q, k, v, uly_out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
@@ -389,7 +403,7 @@ def run_ours(args):
     e_res = tfc_us - ta_us
     hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
-    traffic = recorded_traffic(w["name"])
+    traffic = recorded_traffic(w["name"] + (" causal" if args.causal else ""))
     if uly_ok:
         tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
         uly = {
@@ -413,7 +427,9 @@ def run_ours(args):
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write",
             "timing": "CUDA events on the launch stream around each launch; value = K * flop / sum of times",
-            "call": "xs_attn_a2a_ws (balanced schedule, caller-allocated workspace)",
+            "call": ("xs_attn_causal_a2a (causal, whole-item longest-first schedule)" if args.causal
+                     else "xs_attn_a2a_ws (balanced schedule, caller-allocated workspace)"),
+            "mask": "causal" if args.causal else "none",
         },
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "pct_bf16_peak_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
@@ -424,7 +440,9 @@ def run_ours(args):
         "workspace_bytes": ws_bytes,
         "permute": {"gbs": 2 * nbytes / (tp_us * 1e-6) / 1e9, "frac_hbm": 2 * nbytes / (tp_us * 1e-6) / 1e9 /
                     peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128, scatter> (balanced schedule)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("attn_fwd_kernel<D, scatter, causal>" if args.causal
+                                else "attn_fwd_kernel<D, scatter> (balanced schedule)"),
                      "achieved": kernel_tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic,
@@ -436,7 +454,7 @@ def run_ours(args):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world >= 1:
-        rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds)
+        rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds, causal=args.causal)
         line["cpu_baseline"] = {
             "value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{rows} uniformly drawn query rows of this workload in {wall:.1f} s wall (4*S*D flop per row)"}
@@ -455,6 +473,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--causal", action="store_true",
+                    help="time causal attention (query i sees keys 0..i) instead of full attention")
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="oracle seconds per step for --impl reference (default: sized to the run)")
     args = ap.parse_args(argv)

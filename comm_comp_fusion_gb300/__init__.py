@@ -39,6 +39,7 @@ STATUS_NAMES = {0: "XS_OK", 1: "XS_ERR_NULL", 2: "XS_ERR_SHAPE", 3: "XS_ERR_ALIG
 EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_a2a_permute_inverse", "xs_ulysses_attn",
            "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size", "xs_attn_a2a_noalloc", "xs_last_error",
            "xs_device_status", "xs_selftest_wait_timeout", "xs_version", "xs_attn_a2a_trace", "xs_attn_trace_layout",
+           "xs_attn_causal_a2a", "xs_attn_causal",
            # include/xs_burst.h
            "xs_burst_rec_bytes", "xs_burst_gap")
 
@@ -72,6 +73,10 @@ def _load() -> ctypes.CDLL:
     lib.xs_a2a_permute_inverse.restype = ctypes.c_int
     lib.xs_ulysses_attn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_ulysses_attn.restype = ctypes.c_int
+    lib.xs_attn_causal_a2a.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.xs_attn_causal_a2a.restype = i
+    lib.xs_attn_causal.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.xs_attn_causal.restype = i
     lib.xs_attn_a2a_trace.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_a2a_trace.restype = i
     lib.xs_attn_trace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(sz)]
@@ -198,6 +203,20 @@ def ulysses_attn(q, k, v, out, B, S, H, D, P, scale, workspace=None, workspace_b
     out sequence-partitioned; ``workspace=None`` selects the whole-item schedule."""
     st = lib.xs_ulysses_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
                              _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def attn_causal_a2a(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
+    """Causal attention with the All-to-All scatter (``xs_attn_causal_a2a``); returns the status."""
+    st = lib.xs_attn_causal_a2a(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale),
+                                _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def attn_causal(q, k, v, out, B, S, H, D, P, scale, stream=None, check=True):
+    """Causal attention, head-partitioned output (``xs_attn_causal``); returns the status."""
+    st = lib.xs_attn_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, P, float(scale),
+                            _stream(stream, q, out))
     return _check(st) if check else st
 
 

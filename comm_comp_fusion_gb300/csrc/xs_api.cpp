@@ -177,7 +177,7 @@ std::atomic<uint32_t> g_generation{1};
 // out sequence-partitioned (both All-to-Alls fused; `epi` must be 1).
 xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                          float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0, int layout = 0,
-                         void *trace = nullptr, size_t trace_bytes = 0) {
+                         void *trace = nullptr, size_t trace_bytes = 0, bool causal = false) {
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
@@ -258,8 +258,13 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         p.ws_cnt = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + rec);
         p.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
     }
-    const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr);
+    const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr && !causal);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (causal) {
+        cudaError_t e = xs::launch_causal(D, epi, head_maps, p, grid, s);
+        if (e != cudaSuccess) return fail_cuda("causal attention launch", e);
+        return XS_OK;
+    }
     if (trace) {
         const size_t need = (size_t)grid * p.n_dp * 8 * xs::kTraceWords * 8;
         if (trace_bytes < need)
@@ -310,6 +315,16 @@ xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int
 xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                           float scale, void *workspace, size_t workspace_bytes, void *stream) {
     return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes, 1);
+}
+
+xs_status xs_attn_causal_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                             int P, float scale, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, nullptr, 0, 0, nullptr, 0, true);
+}
+
+xs_status xs_attn_causal(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
+                         float scale, void *stream) {
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0, nullptr, 0, 0, nullptr, 0, true);
 }
 
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,

@@ -59,6 +59,14 @@ cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const Att
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                          cudaStream_t stream) {
+    if (D == 128) return launch_causal_d128(epi, maps, p, grid, stream);
+    if (D == 96) return launch_causal_d96(epi, maps, p, grid, stream);
+    if (D == 64) return launch_causal_d64(epi, maps, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
                            cudaStream_t stream) {
     if (D == 128) return launch_ulysses_d128(maps, p, grid, stream);

@@ -165,7 +165,28 @@ __device__ __forceinline__ void sched_init(Sched &s, const AttnParams &p) {
     s.u = s.u_begin = sk_start(blockIdx.x, p);
     s.u_end = sk_start(blockIdx.x + 1, p);
 }
+// CAU (causal): item lengths differ (pair p needs 2p + 2 K/V tiles), so whole
+// items go out longest first, dealt to the CTAs in a snake order (wave w runs
+// CTA 0..G-1 when w is even and G-1..0 when odd), a longest-processing-time
+// assignment that keeps the CTAs' totals close.
+template <bool CAU>
 __device__ __forceinline__ bool sched_next(Sched &s, const AttnParams &p, Seg &g) {
+    if (CAU) {
+        const int G = (int)gridDim.x, n_heads = p.n_items / p.n_pairs;
+        while (s.k < p.n_dp) {
+            const int w = s.k++;
+            const int rank = w * G + ((w & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+            if (rank >= p.n_items) continue;
+            const int pair = p.n_pairs - 1 - rank / n_heads;
+            g.item = (rank % n_heads) * p.n_pairs + pair;
+            g.j0 = 0;
+            g.j1 = min(2 * pair + 2, p.n_kv);
+            g.split = false;
+            g.first = false;
+            return true;
+        }
+        return false;
+    }
     while (s.k < p.n_dp) {
         const int item = (int)blockIdx.x + s.k * (int)gridDim.x;
         ++s.k;
@@ -193,10 +214,11 @@ __device__ __forceinline__ bool sched_next(Sched &s, const AttnParams &p, Seg &g
 }
 
 // True when the segment just returned by sched_next is this CTA's last.
+template <bool CAU>
 __device__ __forceinline__ bool sched_done(const Sched &s, const AttnParams &p) {
     Sched t = s;
     Seg g;
-    return !sched_next(t, p, g);
+    return !sched_next<CAU>(t, p, g);
 }
 
 // Counts an arrival on a counter stamped with this call's generation (low 12
@@ -479,7 +501,7 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
@@ -540,7 +562,7 @@ __global__ void __launch_bounds__(512, 1)
             Sched sch;
             sched_init(sch, p);
             Seg g;
-            for (; ok && sched_next(sch, p, g); ++it) {
+            for (; ok && sched_next<CAU>(sch, p, g); ++it) {
                 const Item w = decode_item(p, g.item);
                 // sequence-partitioned inputs: batch and global head of the item
                 const int b = LD ? w.rb % p.B : 0, h = LD ? (w.rb / p.B) * p.Hl + w.hl : 0;
@@ -616,8 +638,11 @@ __global__ void __launch_bounds__(512, 1)
             Sched sch;
             sched_init(sch, p);
             Seg g;
-            for (; ok && sched_next(sch, p, g); ++it) {
+            for (; ok && sched_next<CAU>(sch, p, g); ++it) {
                 const int nseg = g.j1 - g.j0;
+                // causal: query tile 0 of pair p stops at its diagonal K/V tile 2p,
+                // one step before tile 1 (which also needs tile 2p + 1)
+                const int n0 = CAU ? min(2 * (g.item % p.n_pairs) + 1, nseg) : nseg;
                 ok = bwait(BAR(BQ_FULL + 0), it & 1u, abort_flag, kSiteMmaQ) &&
                      bwait(BAR(BQ_FULL + 1), it & 1u, abort_flag, kSiteMmaQ);
                 if (!ok) break;
@@ -631,32 +656,34 @@ __global__ void __launch_bounds__(512, 1)
                 issue_S(1, kslot);
                 tc_commit(BAR(BS_FULL + 1));
                 tc_commit(BAR(BKV_EMPTY + kslot));
-                if (nseg == 1) {
-                    tc_commit(BAR(BQ_EMPTY + 0));
-                    tc_commit(BAR(BQ_EMPTY + 1));
-                }
+                if (n0 == 1) tc_commit(BAR(BQ_EMPTY + 0));
+                if (nseg == 1) tc_commit(BAR(BQ_EMPTY + 1));
                 for (int j = 0; j < nseg; ++j) {
                     const uint32_t vslot = kv_it % C::kSlots;
                     ok = bwait(BAR(BKV_FULL + vslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
                     if (!ok) break;
                     ++kv_it;
-                    const bool more = j + 1 < nseg;
+                    const bool more = j + 1 < nseg, more0 = j + 1 < n0;
                     // ---- tile 0: O0 += P0 V_j, then S0 for the next K/V tile
-                    ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
-                    if (ok && j == 0) ok = bwait(BAR(BO_FREE + 0), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
-                    if (!ok) break;
-                    pph0 ^= 1u;
-                    tc_fence_after();
-                    issue_PV(0, vslot, j > 0, 0, 8);
-                    if (!more) tc_commit(BAR(BO_FINAL + 0));
+                    if (!CAU || j < n0) {
+                        ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
+                        if (ok && j == 0) ok = bwait(BAR(BO_FREE + 0), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
+                        if (!ok) break;
+                        pph0 ^= 1u;
+                        tc_fence_after();
+                        issue_PV(0, vslot, j > 0, 0, 8);
+                        if (!more0) tc_commit(BAR(BO_FINAL + 0));
+                    }
                     if (more) {
                         kslot = kv_it % C::kSlots;
                         ok = bwait(BAR(BKV_FULL + kslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
                         if (!ok) break;
                         ++kv_it;
-                        issue_S(0, kslot);
-                        tc_commit(BAR(BS_FULL + 0));
-                        if (j + 2 == nseg) tc_commit(BAR(BQ_EMPTY + 0));
+                        if (more0) {
+                            issue_S(0, kslot);
+                            tc_commit(BAR(BS_FULL + 0));
+                            if (j + 2 == n0) tc_commit(BAR(BQ_EMPTY + 0));
+                        }
                     }
                     // ---- tile 1
                     ok = bwait(BAR(BP_FULL + 1), pph1, abort_flag, kSiteMmaP);
@@ -697,9 +724,11 @@ __global__ void __launch_bounds__(512, 1)
         Sched sch;
         sched_init(sch, p);
         Seg g;
-        for (; ok && sched_next(sch, p, g); ++it) {
+        for (; ok && sched_next<CAU>(sch, p, g); ++it) {
             float m = 0.f, l = 0.f;
-            const int nseg = g.j1 - g.j0;
+            // causal: this tile's diagonal K/V tile (its last step) is 2p + t
+            const int qt_diag = CAU ? 2 * (g.item % p.n_pairs) + t : -1;
+            const int nseg = CAU ? min(qt_diag + 1, g.j1 - g.j0) : g.j1 - g.j0;
             for (int j = 0; j < nseg; ++j) {
                 ok = warp_bwait(BAR(BS_FULL + t), sph, abort_flag, kSiteSoftS);
                 if (!ok) break;
@@ -708,7 +737,7 @@ __global__ void __launch_bounds__(512, 1)
                 // this thread's row of S: columns 0-63 in sa, 64-127 in sb
                 uint32_t sa[64], sb[64];
 #define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
-                if (RAG && g.j0 + j == p.n_kv - 1) {
+                if (RAG && !CAU && g.j0 + j == p.n_kv - 1) {
                     // keys past S (zero-filled rows of the last K/V tile) take no
                     // weight: their scores become -inf in tensor memory
 #pragma unroll 1
@@ -717,6 +746,15 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 tmem_ld64(tS, sa);
                 tmem_ld64(tS + 64, sb);
+                if (CAU && j == qt_diag) {
+                    // the diagonal tile: keys after this row's token take no weight
+                    const uint32_t ninf = f2u(-INFINITY);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        sa[i] = i > row ? ninf : sa[i];
+                        sb[i] = 64 + i > row ? ninf : sb[i];
+                    }
+                }
                 float mx0 = fmaxf(u2f(sa[0]), u2f(sa[1])), mx1 = fmaxf(u2f(sa[2]), u2f(sa[3]));
                 float mx2 = fmaxf(u2f(sa[4]), u2f(sa[5])), mx3 = fmaxf(u2f(sa[6]), u2f(sa[7]));
 #pragma unroll
@@ -792,7 +830,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
             }
             if (!ok) break;
-            if (g.split && sched_done(sch, p)) {
+            if (g.split && sched_done<CAU>(sch, p)) {
                 // This CTA's last piece of a split item: finish tile t here, both
                 // tiles in parallel, instead of handing it to the epilogue. Every
                 // MMA of the CTA is complete once O_t is final, so the query
@@ -835,9 +873,9 @@ __global__ void __launch_bounds__(512, 1)
         Sched sch;
         sched_init(sch, p);
         Seg g;
-        for (; ok && sched_next(sch, p, g); ++it) {
+        for (; ok && sched_next<CAU>(sch, p, g); ++it) {
             // a CTA's last piece of a split item is finished by the softmax warpgroups
-            if (g.split && sched_done(sch, p)) continue;
+            if (g.split && sched_done<CAU>(sch, p)) continue;
             const Item w = decode_item(p, g.item);
             const uint32_t ua = (uint32_t)(g.item - p.sk_item0) * (uint32_t)p.n_kv;  // a split item's first unit
             int c_first = 0, c_last = 0;
@@ -939,10 +977,10 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false>
 static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG>;
+    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
@@ -968,6 +1006,11 @@ static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const A
     cudaError_t launch_ulysses_d##D(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream) {                                                        \
         return launch_t<D, 1, 1>(maps, p, grid, stream);                                                          \
+    }                                                                                                             \
+    cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
+                                   cudaStream_t stream) {                                                         \
+        return epi ? launch_one<D, 1, 0, 0, true, true>(maps, p, grid, stream)                                     \
+                   : launch_one<D, 0, 0, 0, true, true>(maps, p, grid, stream);                                    \
     }                                                                                                             \
     cudaError_t read_error_word_d##D(unsigned int *value, bool clear) {                                           \
         cudaError_t e = cudaMemcpyFromSymbol(value, g_xs_error, sizeof(unsigned int));                            \

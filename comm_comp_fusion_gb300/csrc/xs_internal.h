@@ -72,6 +72,9 @@ cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const A
 // The fused call with epilogue tracing (p.trace set, whole-item schedule).
 cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                     cudaStream_t stream);
+// Causal attention (query token i sees keys 0..i), whole-item schedule.
+cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                          cudaStream_t stream);
 // Sequence-partitioned inputs (the pre-attention All-to-All done by the loads),
 // sequence-partitioned output.
 cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
@@ -83,6 +86,8 @@ cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const Attn
                                       cudaStream_t stream);                                                       \
     cudaError_t launch_ulysses_d##D(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream);                                                         \
+    cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
+                                   cudaStream_t stream);                                                          \
     cudaError_t read_error_word_d##D(unsigned int *value, bool clear);
 XS_DECLARE_ATTN_ENTRY(64)
 XS_DECLARE_ATTN_ENTRY(96)

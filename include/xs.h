@@ -136,6 +136,21 @@ xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out
                           int P, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Causal attention, the autoregressive-LLM case the paper contrasts with DiT's
+ * full attention (section 4.3): query token i of a head attends to key tokens
+ * 0..i of the same sequence only. Same arguments, layouts and rules as
+ * xs_attn_a2a (fused scatter, sequence-partitioned out) and xs_attn
+ * (head-partitioned out); xs_attn_causal_a2a is bit-identical to
+ * xs_a2a_permute(xs_attn_causal(...)). K/V tiles entirely above the diagonal
+ * are skipped; work items (pairs of 128-row query tiles) are dealt longest
+ * first to balance the CTAs.
+ */
+xs_status xs_attn_causal_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                             int P, float scale, void *stream);
+xs_status xs_attn_causal(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
+                         int P, float scale, void *stream);
+
+/*
  * Balanced-schedule variants. Identical results contract and layouts as
  * xs_attn_a2a / xs_attn, plus a caller-owned device workspace that lets the
  * last one to two waves of work be split evenly over all SMs instead of
