@@ -264,10 +264,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ------------------------------------------------------------------ registers
 
+// The attention kernel launches with 128 registers per thread (the build checks
+// this); .inc may only raise a warpgroup's count and .dec only lower it.
+constexpr int kLaunchRegs = 128;
 template <int N> __device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N >= kLaunchRegs && N <= 256 && N % 8 == 0, "setmaxnreg.inc must raise the count");
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N <= kLaunchRegs && N >= 24 && N % 8 == 0, "setmaxnreg.dec must lower the count");
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
