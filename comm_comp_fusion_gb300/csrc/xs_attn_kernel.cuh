@@ -46,6 +46,8 @@
 // shared abort flag, records the site in a device error word and winds down.
 #pragma once
 
+#include <atomic>
+
 #include "xs_internal.h"
 #include "xs_ptx.cuh"
 
@@ -518,6 +520,11 @@ __global__ void __launch_bounds__(512, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // traced instances: per-CTA times after the tile records (kernel entry, set-up
+    // done, first Q load issued, CTA done), %globaltimer
+    unsigned long long *cta_times =
+        TRACE ? p.trace + ((size_t)gridDim.x * p.n_dp * 8 + (size_t)blockIdx.x * 4) * kTraceWords : nullptr;
+    if (TRACE && threadIdx.x == 0) cta_times[0] = globaltimer_ns();
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -552,6 +559,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const int wg = warp >> 2;
+    if (TRACE && threadIdx.x == 0) cta_times[1] = globaltimer_ns();
 
     if (wg == 0) {
         setmaxnreg_dec<48>();
@@ -571,6 +579,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kTile);
                     const int s0 = (2 * w.pair + t) * 128;  // past S for an absent tile: zero fill
+                    if (TRACE && it == 0 && t == 0) cta_times[2] = globaltimer_ns();
                     if (LD) {
                         int rs, sl;
                         seq_position(p, s0, rs, sl);
@@ -974,6 +983,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (TRACE && threadIdx.x == 0) cta_times[3] = globaltimer_ns();
 #undef BAR
 }
 
@@ -981,10 +991,31 @@ template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false>
 static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
     auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
+    // The shared-memory limit is raised once per device and instance: setting a
+    // function attribute before every launch makes each launch start much later.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources) {
+        // the attribute was lost (for instance by a device reset): set it again once
+        configured.fetch_and(~bit, std::memory_order_acq_rel);
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)Cfg<D>::kSmemAlloc)) != cudaSuccess)
+            return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+        kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 // The ragged instances (S not a multiple of 128) carry the key mask and the

@@ -215,7 +215,10 @@ xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void 
  *       before its first global store, clock64 after its last store was issued,
  *       %globaltimer (ns) when ready, and item << 8 | tile << 4 | warp (bit 3
  *       set when the tile is absent: ceil(S/128) odd). Records of a CTA that ran out
- *       of items stay zero. clock64 values compare only within one CTA.
+ *       of items stay zero. clock64 values compare only within one CTA. After
+ *       the records come 20 uint64 per CTA; the first four are the CTA's
+ *       %globaltimer at kernel entry, after set-up (barriers, tensor memory),
+ *       when its first Q load was issued, and when it finished.
  */
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
                             int P, float scale, void *trace, size_t trace_bytes, void *stream);

@@ -79,7 +79,10 @@ def test_trace_matches_untraced_and_covers_tiles(case):
     torch.cuda.synchronize()
     assert xs.device_status() == xs.XS_OK
     assert np.array_equal(from_dev(out), from_dev(ref))
-    r = tr.cpu().numpy().view(np.uint64).reshape(ctas, per, 2, 4, 5)
+    words = tr.cpu().numpy().view(np.uint64)
+    r = words[: ctas * per * 40].reshape(ctas, per, 2, 4, 5)
+    times = words[ctas * per * 40:].reshape(ctas, 20)[:, :4].astype(np.int64)
+    assert (np.diff(times, axis=1) >= 0).all() and (times[:, 0] > 0).all()   # entry <= set-up <= load <= exit
     seen = r[..., 0] != 0
     n_items = P * B * (H // P) * ((S // 128 + 1) // 2)
     assert seen.sum() == n_items * 2 * 4
