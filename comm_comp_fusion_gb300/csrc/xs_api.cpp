@@ -91,7 +91,8 @@ xs_status check_shape(int B, int S, int H, int D, int P, bool attn, size_t *byte
     if (H < 1 || P < 1) return fail(XS_ERR_SHAPE, "H and P must be >= 1 (got H=%d P=%d)", H, P);
     if (H % P) return fail(XS_ERR_SHAPE, "H=%d is not a multiple of P=%d", H, P);
     if (S % P) return fail(XS_ERR_SHAPE, "S=%d is not a multiple of P=%d", S, P);
-    if (D != 64 && D != 96 && D != 128) return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64, 96 or 128)", D);
+    if (D != 64 && D != 96 && D != 128 && D != 256)
+        return fail(XS_ERR_UNSUPPORTED, "D=%d is not supported (64, 96, 128 or 256)", D);
     const unsigned long long rows = (unsigned long long)B * S * H;
     if (rows >= (1ull << 31)) return fail(XS_ERR_SHAPE, "B*S*H=%llu rows exceeds 2^31-1", rows);
     *bytes = (size_t)rows * D * 2;
@@ -239,7 +240,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     p.n_pairs = (p.n_qt + 1) / 2;
     p.n_kv = (S + 127) / 128;
     p.kv_tail = S - (p.n_kv - 1) * 128;
-    const long long items = (long long)P * B * p.Hl * p.n_pairs;
+    const long long items = (long long)P * B * p.Hl * (xs::single_tile_items(D) ? p.n_qt : p.n_pairs);
     if (items >= (1ll << 31)) return fail(XS_ERR_SHAPE, "too many work items (%lld)", items);
     p.n_items = (int)items;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
@@ -371,7 +372,7 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
     DeviceInfo info;
     if ((st = current_device(&dev, &info))) return st;
     const int n_qt = (S + 127) / 128;
-    const long long n_items = (long long)P * B * (H / P) * ((n_qt + 1) / 2);
+    const long long n_items = (long long)P * B * (H / P) * (xs::single_tile_items(D) ? n_qt : (n_qt + 1) / 2);
     *bytes = xs::attn_workspace_bytes((int)n_items, n_qt, D, info.num_sms);
     return XS_OK;
 }
@@ -396,7 +397,7 @@ xs_status permute_call(const void *in, void *out, int B, int S, int H, int D, in
     xs::PermParams p;
     p.rows = (uint32_t)((unsigned long long)B * S * H);
     p.cpr = (uint32_t)(D / 8);
-    p.cpr_log2 = D == 128 ? 4u : 3u;
+    p.cpr_log2 = D == 256 ? 5u : D == 128 ? 4u : 3u;
     xs::fastdiv_magic(p.cpr, &p.mC, &p.sC);
     if (D == 96 && (unsigned long long)p.rows * p.cpr >= (1ull << 31))
         return fail(XS_ERR_SHAPE, "a D=96 permute handles at most 2^31 16-byte chunks (tensor below 32 GiB)");

@@ -1,6 +1,6 @@
 // xs_attn.cu -- host side of the attention kernel: the work schedule, the
 // workspace size, dispatch to the per-head-dimension instances
-// (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu), the bounded-wait
+// (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu, xs_attn_d256.cu), the bounded-wait
 // self-test and the device error words.
 #include "xs_attn_kernel.cuh"
 
@@ -41,12 +41,14 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     (void)n_kv;
     const size_t rec = ((size_t)2 * num_sms * partial_record_bytes(D) + 255) & ~(size_t)255;
-    const size_t cnt = ((size_t)n_items * 8 * sizeof(uint32_t) + 255) & ~(size_t)255;
+    // four epilogue warps' arrival counters per tile
+    const size_t cnt = ((size_t)n_items * 4 * tiles_per_item(D) * sizeof(uint32_t) + 255) & ~(size_t)255;
     return rec + cnt;
 }
 
 cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                              cudaStream_t stream) {
+    if (D == 256) return launch_attention_d256(epi, maps, p, grid, stream);
     if (D == 128) return launch_attention_d128(epi, maps, p, grid, stream);
     if (D == 96) return launch_attention_d96(epi, maps, p, grid, stream);
     if (D == 64) return launch_attention_d64(epi, maps, p, grid, stream);
@@ -61,6 +63,7 @@ cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const Att
 
 cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                           cudaStream_t stream) {
+    if (D == 256) return launch_causal_d256(epi, maps, p, grid, stream);
     if (D == 128) return launch_causal_d128(epi, maps, p, grid, stream);
     if (D == 96) return launch_causal_d96(epi, maps, p, grid, stream);
     if (D == 64) return launch_causal_d64(epi, maps, p, grid, stream);
@@ -69,6 +72,7 @@ cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const Attn
 
 cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
                            cudaStream_t stream) {
+    if (D == 256) return launch_ulysses_d256(maps, p, grid, stream);
     if (D == 128) return launch_ulysses_d128(maps, p, grid, stream);
     if (D == 96) return launch_ulysses_d96(maps, p, grid, stream);
     if (D == 64) return launch_ulysses_d64(maps, p, grid, stream);
@@ -113,7 +117,7 @@ cudaError_t read_device_error(unsigned int *value, bool clear, cudaStream_t stre
         if ((e = cudaMemcpyToSymbol(g_xs_error, &zero, sizeof(unsigned int))) != cudaSuccess) return e;
     }
     cudaError_t (*const per_d[])(unsigned int *, bool) = {read_error_word_d64, read_error_word_d96,
-                                                          read_error_word_d128};
+                                                          read_error_word_d128, read_error_word_d256};
     for (auto fn : per_d) {
         if ((e = fn(&w, clear)) != cudaSuccess) return e;
         all |= w;

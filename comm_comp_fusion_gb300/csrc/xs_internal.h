@@ -26,7 +26,7 @@ struct AttnParams {
     int n_pairs;  // work items per head           (ceil(n_qt / 2))
     int n_kv;     // 128-row K/V tiles per head    (ceil(S / 128))
     int kv_tail;  // keys in the last K/V tile (128 unless S is ragged); later columns are masked
-    int n_items;  // P * B * Hl * n_pairs
+    int n_items;  // P * B * Hl * n_pairs (P * B * Hl * n_qt for single-tile items)
     float scale_log2;  // scale * log2(e): softmax runs in base 2
     uint16_t *out;
     int n_dp;              // round-robin waves of whole items
@@ -45,9 +45,16 @@ struct AttnParams {
 // item << 8 | tile << 4 | warp, with bit 3 set for an absent tile.
 constexpr int kTraceWords = 5;
 
-// Bytes of one partial record: unnormalised O of both tiles (fp32) plus the
-// row max and row sum of both tiles.
-inline size_t partial_record_bytes(int D) { return (size_t)2 * 128 * D * 4 + (size_t)2 * 2 * 128 * 4; }
+// Head dimension 256 runs the single-query-tile kernel (xs_attn1_kernel.cuh):
+// its work item is one 128-row query tile instead of a pair.
+inline bool single_tile_items(int D) { return D > 128; }
+inline int tiles_per_item(int D) { return single_tile_items(D) ? 1 : 2; }
+
+// Bytes of one partial record: unnormalised O of the item's tiles (fp32) plus
+// their row max and row sum.
+inline size_t partial_record_bytes(int D) {
+    return (size_t)tiles_per_item(D) * (128 * (size_t)D * 4 + 2 * 128 * 4);
+}
 
 // Chooses the grid and fills the schedule fields of p. With a workspace the
 // tail waves are balanced; without one every CTA takes whole items only.
@@ -92,6 +99,7 @@ cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const Attn
 XS_DECLARE_ATTN_ENTRY(64)
 XS_DECLARE_ATTN_ENTRY(96)
 XS_DECLARE_ATTN_ENTRY(128)
+XS_DECLARE_ATTN_ENTRY(256)
 cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                          cudaStream_t stream);
 

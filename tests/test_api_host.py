@@ -72,8 +72,8 @@ def test_attention_argument_checks(xs, fn_name):
     assert _attn(xs, fn, scale=float("inf")) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, scale=0.0) == xs.XS_ERR_SHAPE
     assert _attn(xs, fn, scale=-0.125) == xs.XS_ERR_SHAPE
-    assert _attn(xs, fn, D=256) == xs.XS_ERR_UNSUPPORTED
-    assert "D=256" in xs.last_error()
+    assert _attn(xs, fn, D=512) == xs.XS_ERR_UNSUPPORTED
+    assert "D=512" in xs.last_error()
     assert _attn(xs, fn, D=80) == xs.XS_ERR_UNSUPPORTED
     assert _attn(xs, fn, q=Q + 8) == xs.XS_ERR_ALIGN
     assert _attn(xs, fn, o=O + 2) == xs.XS_ERR_ALIGN
@@ -110,7 +110,7 @@ def test_ulysses_argument_checks(xs):
     assert f(H=6) == xs.XS_ERR_SHAPE
     assert f(S=202) == xs.XS_ERR_SHAPE                  # S % P
     assert f(S=100) == xs.XS_ERR_UNSUPPORTED            # Sl = 25 is not a multiple of 8
-    assert f(D=256) == xs.XS_ERR_UNSUPPORTED
+    assert f(D=512) == xs.XS_ERR_UNSUPPORTED
     assert f(P=16, H=16) == xs.XS_ERR_UNSUPPORTED and "P=16" in xs.last_error()
     assert f(o=Q + 32) == xs.XS_ERR_ALIAS
     assert f(o=O + 8) == xs.XS_ERR_ALIGN

@@ -120,7 +120,7 @@ def test_many_items_per_cta():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, 6, 7])
 def test_workload_full_size(idx):
     """Full-size workloads in the bench's launch configuration: sampled rows against
     the oracle, the whole output fused vs unfused bit for bit."""

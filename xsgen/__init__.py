@@ -90,6 +90,8 @@ WORKLOADS = [
          name="ragged DiT: B=1 S=4032 H=24 D=128 P=8"),
     dict(B=1, S=8192, H=32, D=96, P=8, sigma_qk=1.0, sigma_v=1.0, scale=96 ** -0.5,
          name="D=96: B=1 S=8192 H=32 D=96 P=8"),
+    dict(B=1, S=8192, H=16, D=256, P=8, sigma_qk=1.0, sigma_v=1.0, scale=256 ** -0.5,
+         name="D=256: B=1 S=8192 H=16 D=256 P=8"),
 ]
 
 
