@@ -267,7 +267,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         return XS_OK;
     }
     if (trace) {
-        const size_t need = ((size_t)grid * p.n_dp * 8 + (size_t)grid * 4) * xs::kTraceWords * 8;
+        const size_t need = ((size_t)grid * p.n_dp * 8 + (size_t)grid * 4) * xs::kTraceWords * 8 + 2 * 2 * 64 * 4 * 8;
         if (trace_bytes < need)
             return fail(XS_ERR_SHAPE, "trace buffer of %zu bytes is smaller than the %zu bytes needed", trace_bytes,
                         need);
@@ -355,7 +355,7 @@ xs_status xs_attn_trace_layout(int B, int S, int H, int D, int P, int *ctas, int
     const int grid = xs::attn_schedule(p, info.num_sms, false);
     *ctas = grid;
     *items_per_cta = p.n_dp;
-    *bytes = ((size_t)grid * p.n_dp * 8 + (size_t)grid * 4) * xs::kTraceWords * 8;
+    *bytes = ((size_t)grid * p.n_dp * 8 + (size_t)grid * 4) * xs::kTraceWords * 8 + 2 * 2 * 64 * 4 * 8;
     return XS_OK;
 }
 

@@ -524,6 +524,17 @@ __global__ void __launch_bounds__(512, 1)
     // done, first Q load issued, CTA done), %globaltimer
     unsigned long long *cta_times =
         TRACE ? p.trace + ((size_t)gridDim.x * p.n_dp * 8 + (size_t)blockIdx.x * 4) * kTraceWords : nullptr;
+    // and, for CTA 0's first two items, per tile and K/V step (up to 64): clock64
+    // when the softmax saw S ready, when it handed P over, when the MMA issuer
+    // saw P complete, and after it issued that P V
+    unsigned long long *step_times =
+        TRACE && blockIdx.x == 0 ? p.trace + ((size_t)gridDim.x * p.n_dp * 8 + (size_t)gridDim.x * 4) * kTraceWords
+                                 : nullptr;
+#define STEP_TIME(item, t, j, k, v)                                                              \
+    do {                                                                                         \
+        if (TRACE && step_times && (item) < 2 && (j) < 64)                                       \
+            step_times[(((size_t)(item) * 2 + (t)) * 64 + (size_t)(j)) * 4 + (k)] = (v);          \
+    } while (0)
     if (TRACE && threadIdx.x == 0) cta_times[0] = globaltimer_ns();
 
     if (threadIdx.x == 0) {
@@ -676,11 +687,13 @@ __global__ void __launch_bounds__(512, 1)
                     // ---- tile 0: O0 += P0 V_j, then S0 for the next K/V tile
                     if (!CAU || j < n0) {
                         ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
+                        STEP_TIME(it, 0, j, 2, clock64_now());
                         if (ok && j == 0) ok = bwait(BAR(BO_FREE + 0), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
                         if (!ok) break;
                         pph0 ^= 1u;
                         tc_fence_after();
                         issue_PV(0, vslot, j > 0, 0, 8);
+                        STEP_TIME(it, 0, j, 3, clock64_now());
                         if (!more0) tc_commit(BAR(BO_FINAL + 0));
                     }
                     if (more) {
@@ -696,11 +709,13 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     // ---- tile 1
                     ok = bwait(BAR(BP_FULL + 1), pph1, abort_flag, kSiteMmaP);
+                    STEP_TIME(it, 1, j, 2, clock64_now());
                     if (ok && j == 0) ok = bwait(BAR(BO_FREE + 1), (it & 1u) ^ 1u, abort_flag, kSiteMmaOFree);
                     if (!ok) break;
                     pph1 ^= 1u;
                     tc_fence_after();
                     issue_PV(1, vslot, j > 0, 0, 8);
+                    STEP_TIME(it, 1, j, 3, clock64_now());
                     tc_commit(BAR(BKV_EMPTY + vslot));
                     if (!more) tc_commit(BAR(BO_FINAL + 1));
                     if (more) {
@@ -741,6 +756,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int j = 0; j < nseg; ++j) {
                 ok = warp_bwait(BAR(BS_FULL + t), sph, abort_flag, kSiteSoftS);
                 if (!ok) break;
+                if (TRACE && (warp & 3) == 0 && lane == 0) STEP_TIME(it, t, j, 0, clock64_now());
                 sph ^= 1u;
                 tc_fence_after();
                 // this thread's row of S: columns 0-63 in sa, 64-127 in sb
@@ -836,6 +852,7 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
+                if (TRACE && (warp & 3) == 0 && lane == 0) STEP_TIME(it, t, j, 1, clock64_now());
                 if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
             }
             if (!ok) break;
@@ -984,6 +1001,7 @@ __global__ void __launch_bounds__(512, 1)
         tmem_dealloc(tmem, C::kTmemCols);
     }
     if (TRACE && threadIdx.x == 0) cta_times[3] = globaltimer_ns();
+#undef STEP_TIME
 #undef BAR
 }
 

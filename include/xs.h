@@ -218,7 +218,11 @@ xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void 
  *       of items stay zero. clock64 values compare only within one CTA. After
  *       the records come 20 uint64 per CTA; the first four are the CTA's
  *       %globaltimer at kernel entry, after set-up (barriers, tensor memory),
- *       when its first Q load was issued, and when it finished.
+ *       when its first Q load was issued, and when it finished. Last come
+ *       [2 items][2 tiles][64 K/V steps][4] uint64 for CTA 0's first two items:
+ *       clock64 when the softmax's first warp saw the step's scores ready,
+ *       when it handed P over, when the MMA issuer saw P complete, and after
+ *       it issued that P V.
  */
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
                             int P, float scale, void *trace, size_t trace_bytes, void *stream);

@@ -81,7 +81,12 @@ def test_trace_matches_untraced_and_covers_tiles(case):
     assert np.array_equal(from_dev(out), from_dev(ref))
     words = tr.cpu().numpy().view(np.uint64)
     r = words[: ctas * per * 40].reshape(ctas, per, 2, 4, 5)
-    times = words[ctas * per * 40:].reshape(ctas, 20)[:, :4].astype(np.int64)
+    times = words[ctas * per * 40: ctas * per * 40 + ctas * 20].reshape(ctas, 20)[:, :4].astype(np.int64)
+    steps = words[ctas * per * 40 + ctas * 20:].reshape(2, 2, 64, 4).astype(np.int64)
+    done = steps[..., 3] != 0   # CTA 0's steps: S seen <= P handed over <= P seen by the MMA <= P V issued
+    assert done.any()
+    s = steps[done]
+    assert (s[:, 0] <= s[:, 1]).all() and (s[:, 1] <= s[:, 2] + 200).all() and (s[:, 2] <= s[:, 3]).all()
     assert (np.diff(times, axis=1) >= 0).all() and (times[:, 0] > 0).all()   # entry <= set-up <= load <= exit
     seen = r[..., 0] != 0
     n_items = P * B * (H // P) * ((S // 128 + 1) // 2)
