@@ -62,6 +62,12 @@ def _load():
         lib.xs_oracle_attention_rows_ex.restype = ci
         lib.xs_oracle_attention_a2a_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
         lib.xs_oracle_attention_a2a_ex.restype = ci
+        lib.xs_oracle_e4m3_decode.argtypes = [vp, vp, i64]
+        lib.xs_oracle_e4m3_decode.restype = ci
+        lib.xs_oracle_attention_q8.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
+        lib.xs_oracle_attention_q8.restype = ci
+        lib.xs_oracle_attention_rows_q8.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, vp, i64, vp, ci]
+        lib.xs_oracle_attention_rows_q8.restype = ci
         lib.xs_oracle_a2a.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
         lib.xs_oracle_a2a.restype = ctypes.c_int
         lib.xs_oracle_a2a_inverse.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
@@ -121,6 +127,41 @@ def attention_a2a(q, k, v, B, S, H, D, P, scale, nthreads=0, causal=False):
     out = np.empty((P, B, S // P, H, D), dtype=np.float64)
     _check(_load().xs_oracle_attention_a2a_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data,
                                               out.ctypes.data, B, S, H, D, P, float(scale), int(causal), nthreads))
+    return out
+
+
+def _u8(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("E4M3 inputs are bytes (numpy uint8)")
+    return a
+
+
+def e4m3_decode(codes):
+    """OFP8 E4M3 bytes -> float64 values (NaN for the NaN codes)."""
+    codes = _u8(codes)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _check(_load().xs_oracle_e4m3_decode(codes.ctypes.data, out.ctypes.data, codes.size))
+    return out
+
+
+def attention_q8(q8, k8, v, B, S, H, D, P, scale, causal=False, nthreads=0):
+    """Head-partitioned fp64 attention with q and k given as E4M3 bytes, v bf16."""
+    q8, k8, v = _u8(q8), _u8(k8), _u16(v)
+    out = np.empty((P, B, S, H // P, D), dtype=np.float64)
+    _check(_load().xs_oracle_attention_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, out.ctypes.data,
+                                          B, S, H, D, P, float(scale), int(causal), nthreads))
+    return out
+
+
+def attention_rows_q8(q8, k8, v, B, S, H, D, P, scale, rows, causal=False, nthreads=0):
+    """fp64 attention with E4M3 q and k for selected head-partitioned rows -> [n][D]."""
+    q8, k8, v = _u8(q8), _u8(k8), _u16(v)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, D), dtype=np.float64)
+    _check(_load().xs_oracle_attention_rows_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, B, S, H, D, P,
+                                               float(scale), int(causal), rows.ctypes.data, rows.size,
+                                               out.ctypes.data, nthreads))
     return out
 
 

@@ -23,6 +23,13 @@
  *    out). Reading taken: query token i of a head sees key tokens j <= i of the
  *    same sequence, so every sum above runs over j = 0..i instead of 0..S-1.
  *
+ *  - FP8 query/key inputs (an extension; the pages evaluate bf16 only): q and k
+ *    may be given as E4M3 bytes, the format of the OCP 8-bit floating point
+ *    specification (OFP8): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *    bits; exponent field 0 holds subnormals m/8 * 2^-6; S.1111.111 is NaN and
+ *    there is no infinity (largest finite 1.75 * 2^8 = 448). They are widened
+ *    exactly to double and the attention above is unchanged.
+ *
  *  - Ulysses post-attention All-to-All (section 4.3, Figure 5 d-e): attention
  *    runs head-partitioned (rank r holds heads r*Hl .. r*Hl+Hl-1 for all S
  *    tokens); the All-to-All restores the sequence partition (rank r' holds
@@ -52,6 +59,25 @@ static double bf16_to_double(uint16_t h) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* OFP8 E4M3 code -> value (NaN for the two NaN codes). */
+static double e4m3_to_double(uint8_t x) {
+    const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+int xs_oracle_e4m3_decode(const uint8_t *in, double *out, int64_t n) {
+    if (n < 0 || (n && (!in || !out))) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(in[i]);
+    return 0;
 }
 
 static int check_shape(int64_t B, int64_t S, int64_t H, int64_t D, int64_t P) {
@@ -135,6 +161,7 @@ int xs_oracle_a2a_inverse(const void *in, void *out, int64_t B, int64_t S, int64
 
 typedef struct {
     const uint16_t *q, *k, *v;
+    const uint8_t *q8, *k8;  /* E4M3 q and k instead of q and k when not NULL */
     int64_t B, S, H, D, P;
     double scale;
     int causal;        /* 1: query token i sees keys 0..i only */
@@ -156,16 +183,23 @@ static void attend_row(const attn_job_t *j, int64_t row, double *p, double *qi, 
     const int64_t head_base = (rb * S * Hl + hl) * D;
     const int64_t row_stride = Hl * D;
 
-    for (int64_t d = 0; d < D; ++d) qi[d] = bf16_to_double(j->q[head_base + s_i * row_stride + d]);
+    for (int64_t d = 0; d < D; ++d)
+        qi[d] = j->q8 ? e4m3_to_double(j->q8[head_base + s_i * row_stride + d])
+                      : bf16_to_double(j->q[head_base + s_i * row_stride + d]);
 
     /* the keys this query sees: all S, or 0..s_i when causal */
     const int64_t t0 = 0, t1 = j->causal ? s_i + 1 : S;
 
     /* scores s_j = scale * <q_i, k_j> */
     for (int64_t t = t0; t < t1; ++t) {
-        const uint16_t *kt = j->k + head_base + t * row_stride;
         double acc = 0.0;
-        for (int64_t d = 0; d < D; ++d) acc += qi[d] * bf16_to_double(kt[d]);
+        if (j->k8) {
+            const uint8_t *kt = j->k8 + head_base + t * row_stride;
+            for (int64_t d = 0; d < D; ++d) acc += qi[d] * e4m3_to_double(kt[d]);
+        } else {
+            const uint16_t *kt = j->k + head_base + t * row_stride;
+            for (int64_t d = 0; d < D; ++d) acc += qi[d] * bf16_to_double(kt[d]);
+        }
         p[t] = j->scale * acc;
     }
     /* m = max_j s_j */
@@ -246,7 +280,18 @@ int xs_oracle_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t 
     int64_t total = P * B * S * (H / P);
     if (total == 0) return 1;
     if (!q || !k || !v || !o) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
+    attn_job_t base = {q, k, v, 0, 0, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
+    return run_attention(base, total, nthreads);
+}
+
+/* As xs_oracle_attention_ex with q and k given as E4M3 bytes (same layout). */
+int xs_oracle_attention_q8(const uint8_t *q8, const uint8_t *k8, const uint16_t *v, double *o, int64_t B, int64_t S,
+                           int64_t H, int64_t D, int64_t P, double scale, int causal, int nthreads) {
+    if (check_shape(B, S, H, D, P)) return XSO_EINVAL;
+    int64_t total = P * B * S * (H / P);
+    if (total == 0) return 1;
+    if (!q8 || !k8 || !v || !o) return XSO_EINVAL;
+    attn_job_t base = {0, 0, v, q8, k8, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
     return run_attention(base, total, nthreads);
 }
 
@@ -265,7 +310,20 @@ int xs_oracle_attention_rows_ex(const uint16_t *q, const uint16_t *k, const uint
     int64_t total_rows = P * B * S * (H / P);
     for (int64_t i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total_rows) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
+    attn_job_t base = {q, k, v, 0, 0, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
+    return run_attention(base, nrows, nthreads);
+}
+
+int xs_oracle_attention_rows_q8(const uint8_t *q8, const uint8_t *k8, const uint16_t *v, int64_t B, int64_t S,
+                                int64_t H, int64_t D, int64_t P, double scale, int causal, const int64_t *rows,
+                                int64_t nrows, double *o_rows, int nthreads) {
+    if (check_shape(B, S, H, D, P) || nrows < 0) return XSO_EINVAL;
+    if (nrows == 0) return 1;
+    if (!q8 || !k8 || !v || !rows || !o_rows) return XSO_EINVAL;
+    int64_t total_rows = P * B * S * (H / P);
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= total_rows) return XSO_EINVAL;
+    attn_job_t base = {0, 0, v, q8, k8, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
     return run_attention(base, nrows, nthreads);
 }
 

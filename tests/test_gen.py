@@ -42,3 +42,14 @@ def test_bf16_rounding_helpers():
     bits = xsgen.f32_to_bf16_bits(x)
     # ties go to even: 1 + 2^-8 -> 1.0, 1 + 3*2^-8 -> 1 + 2^-6
     assert xsgen.bf16_bits_to_f32(bits).tolist()[:4] == [1.0, 1.0, 1.0 + 2 ** -6, -2.5]
+
+
+def test_e4m3_encoder_rounds_to_nearest_even():
+    vals = {0.0: 0x00, 1.0: 0x38, -1.0: 0xB8, 448.0: 0x7E, 1000.0: 0x7E, -1e9: 0xFE, 0.015625: 0x08}
+    got = xsgen.f32_to_e4m3(np.array(list(vals)))
+    assert got.tolist() == list(vals.values())
+    # halfway between 1.0 (0x38) and 1.125 (0x39): ties to the even code 0x38;
+    # halfway between 1.125 and 1.25 (0x3A): to 0x3A
+    assert xsgen.f32_to_e4m3(np.array([1.0625, 1.1875])).tolist() == [0x38, 0x3A]
+    x = xsgen.normal_e4m3(5, 1, (4096,))
+    assert x.dtype == np.uint8 and (x & 0x7F).max() <= 0x7E

@@ -169,6 +169,43 @@ def test_causal_rows_and_a2a_apis_agree():
                                   oracle.a2a(full, B, S, H, D, P))
 
 
+# ------------------------------------------------------------------ FP8 inputs
+
+def test_e4m3_decode_standard_values():
+    g = json.load(open(os.path.join(GOLDEN, "e4m3_values.json")))["values"]
+    codes = np.array([int(c, 16) for c in g], dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    for c, want, v in zip(g, g.values(), got):
+        if want == "nan":
+            assert math.isnan(v), c
+        else:
+            assert v == want and math.copysign(1.0, v) == math.copysign(1.0, want), c
+
+
+def test_e4m3_codes_are_ordered_and_symmetric():
+    pos = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    assert (np.diff(pos) > 0).all()
+    neg = oracle.e4m3_decode(np.arange(0x80, 0xFF, dtype=np.uint8))
+    np.testing.assert_array_equal(neg, -pos)
+
+
+def test_attention_q8_equals_bf16_on_widened_inputs():
+    """Every E4M3 value is exact in bf16, so attention on E4M3 q and k must equal
+    the (separately pinned) bf16 attention on their widened values, bit for bit."""
+    B, S, H, D, P = 2, 12, 4, 8, 2
+    q8 = xsgen.normal_e4m3(21, 1, (P, B, S, H // P, D), 2.0)
+    k8 = xsgen.normal_e4m3(21, 2, (P, B, S, H // P, D), 2.0)
+    _, _, v = xsgen.random_inputs(21, P, B, S, H, D)
+    widen = lambda c: xsgen.f32_to_bf16_bits(oracle.e4m3_decode(c).astype(np.float32))
+    for causal in (False, True):
+        a = oracle.attention_q8(q8, k8, v, B, S, H, D, P, 0.3, causal=causal)
+        b = oracle.attention(widen(q8), widen(k8), v, B, S, H, D, P, 0.3, causal=causal)
+        np.testing.assert_array_equal(a, b)
+    rows = np.array([0, 7, 30, P * B * S * (H // P) - 1])
+    np.testing.assert_array_equal(oracle.attention_rows_q8(q8, k8, v, B, S, H, D, P, 0.3, rows),
+                                  oracle.attention(widen(q8), widen(k8), v, B, S, H, D, P, 0.3).reshape(-1, D)[rows])
+
+
 # ------------------------------------------------------------------ invariants
 
 def test_rows_are_probabilities():
@@ -317,6 +354,9 @@ _MUTANTS = {
     "causal looks ahead": ("const int64_t t0 = 0, t1 = j->causal ? s_i + 1 : S;",
                            "const int64_t t0 = j->causal ? s_i : 0, t1 = S;"),
     "causal mask ignored": ("j->causal ? s_i + 1 : S", "S"),
+    "e4m3 exponent bias": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3 subnormal scale": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "e4m3 mantissa width": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 16.0, e - 7);"),
 }
 
 
@@ -340,7 +380,13 @@ def _pins_pass(lib):
                                    B, S, H, D, P, sc, 1, 2)
         return o
 
-    ok = True
+    lib.xs_oracle_e4m3_decode.argtypes = [vp, vp, i64]
+    g8 = json.load(open(os.path.join(GOLDEN, "e4m3_values.json")))["values"]
+    codes = np.array([int(c, 16) for c in g8], dtype=np.uint8)
+    dec = np.empty(codes.size)
+    lib.xs_oracle_e4m3_decode(codes.ctypes.data, dec.ctypes.data, codes.size)
+    want = np.array([np.nan if x == "nan" else x for x in g8.values()])
+    ok = bool(np.array_equal(np.isnan(dec), np.isnan(want)) and np.array_equal(dec[~np.isnan(want)], want[~np.isnan(want)]))
     B, S, H, D, P, scale, sigma = TINY[3]
     q, k, v = xsgen.random_inputs(91 + S * 10 + D, P, B, S, H, D, sigma, 1.0)
     ok &= bool(np.allclose(attn_causal(q, k, v, B, S, H, D, P, scale),

@@ -112,3 +112,34 @@ def random_inputs(seed: int, P: int, B: int, S: int, H: int, D: int, sigma_qk: f
     return (normal_bf16(seed, 1, shape, sigma_qk, nthreads),
             normal_bf16(seed, 2, shape, sigma_qk, nthreads),
             normal_bf16(seed, 3, shape, sigma_v, nthreads))
+
+
+# ------------------------------------------------------------ FP8 (E4M3) inputs
+# OFP8 E4M3 (OCP 8-bit floating point specification): 1 sign bit, 4 exponent
+# bits with bias 7, 3 mantissa bits, subnormals at exponent field 0, no
+# infinities, S.1111.111 is NaN. Used only to turn the seeded normal draws into
+# E4M3 bytes; the oracle decodes bytes with its own implementation.
+
+def _e4m3_positive_values() -> np.ndarray:
+    codes = np.arange(0x7F)
+    e, m = codes >> 3, codes & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest finite E4M3 value (ties to the even code), saturating
+    at +-448; returns the bytes (uint8)."""
+    x = np.asarray(x, dtype=np.float64)
+    vals = _e4m3_positive_values()
+    a = np.minimum(np.abs(x), vals[-1])
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return (code | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)).astype(np.uint8)
+
+
+def normal_e4m3(seed: int, stream: int, shape, sigma: float = 1.0, nthreads: int = 0) -> np.ndarray:
+    """E4M3 bytes of the seeded sigma * N(0,1) draw (its bf16 value rounded to E4M3)."""
+    return f32_to_e4m3(bf16_bits_to_f32(normal_bf16(seed, stream, shape, sigma, nthreads)))
