@@ -24,6 +24,9 @@ the post-attention permute); it is reported under ``ulysses``. ``e2e``
 times the same call with the inputs copied in from pinned host memory and the
 output copied back inside the timed region.
 
+--q8 times the E4M3 query/key call (xs_attn_a2a_q8) on the same draws
+rounded to E4M3; v and the output stay bf16.
+
 --impl reference times the fp64 CPU oracle (the checker of this library, not
 a tuned CPU implementation) on the host cores over a bounded sample of query
 rows of the same workload; it runs on rank 0 only.
@@ -72,6 +75,12 @@ def workload_flops(w, causal: bool = False) -> float:
     over S * S pairs per (b, h), or the S * (S + 1) / 2 pairs j <= i when causal."""
     pairs = w["S"] * (w["S"] + 1) / 2.0 if causal else float(w["S"]) * w["S"]
     return 4.0 * w["B"] * w["H"] * pairs * w["D"]
+
+
+def e4m3_inputs(x):
+    """E4M3 bytes of a bf16 operand (nearest value, saturating at 448)."""
+    import xsgen
+    return xsgen.f32_to_e4m3(xsgen.bf16_bits_to_f32(x))
 
 
 def workload_bytes(w) -> int:
@@ -181,23 +190,29 @@ def barrier(world: int):
 
 # --------------------------------------------------------------- CPU oracle leg
 
-def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0, causal: bool = False):
-    """Times the fp64 oracle on about `seconds` of sampled query rows of workload w.
-    Returns (tflops, rows, wall_s, threads)."""
+def oracle_rows_rate(w, q, k, v, seconds: float, seed: int = 0, causal: bool = False, q8: bool = False):
+    """Times the fp64 oracle on about `seconds` of sampled query rows of workload w
+    (q, k as E4M3 bytes when q8). Returns (tflops, rows, wall_s, threads)."""
     import numpy as np
     import oracle
     B, S, H, D, P = w["B"], w["S"], w["H"], w["D"], w["P"]
     total_rows = P * B * S * (H // P)
     rng = np.random.default_rng(seed)
     threads = oracle.default_threads()
+    if q8:
+        rows_fn = lambda r: (oracle.attention_rows_q8(q, k, v, B, S, H, D, P, w["scale"], r, causal=causal),
+                             threads)
+    else:
+        rows_fn = lambda r: oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], r, return_threads=True,
+                                                  causal=causal)
     probe = rng.integers(0, total_rows, max(threads, 16))
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], probe, causal=causal)
+    rows_fn(probe)
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(max(threads, min(total_rows, len(probe) * seconds / dt)))
     rows = rng.integers(0, total_rows, n)
     t0 = time.perf_counter()
-    _, used = oracle.attention_rows(q, k, v, B, S, H, D, P, w["scale"], rows, return_threads=True, causal=causal)
+    _, used = rows_fn(rows)
     wall = time.perf_counter() - t0
     # a row of token s sees S keys, or s + 1 when causal: 4 * D flop per key
     keys = (((rows // (H // P)) % S) + 1).sum() if causal else S * n
@@ -212,13 +227,15 @@ def run_reference(args):
     import xsgen
     w = xsgen.WORKLOADS[args.workload]
     q, k, v = xsgen.workload_inputs(args.workload)
+    if args.q8:
+        q, k = e4m3_inputs(q), e4m3_inputs(k)
     # Each step is a bounded sample so that warm-up plus K steps stay within a few minutes.
     per_step = args.ref_step_seconds or max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
-        oracle_rows_rate(w, q, k, v, per_step / 4, seed=100 + i, causal=args.causal)
+        oracle_rows_rate(w, q, k, v, per_step / 4, seed=100 + i, causal=args.causal, q8=args.q8)
     flop_total, rows_total, wall_total, threads = 0.0, 0, 0.0, 0
     for i in range(args.steps):
-        r, n, wall, threads = oracle_rows_rate(w, q, k, v, per_step, seed=i, causal=args.causal)
+        r, n, wall, threads = oracle_rows_rate(w, q, k, v, per_step, seed=i, causal=args.causal, q8=args.q8)
         flop_total += r * 1e12 * wall
         rows_total += n
         wall_total += wall
@@ -232,6 +249,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "S": w["S"], "H": w["H"], "D": w["D"], "P": w["P"],
                    "parallelism": "replicas", "mask": "causal" if args.causal else "none",
+                   "inputs": "q, k E4M3, v bf16" if args.q8 else "q, k, v bf16",
                    "what": "fp64 CPU oracle (two-pass softmax attention per row)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -264,8 +282,11 @@ def run_ours(args):
     nbytes = workload_bytes(w)
     flops = workload_flops(w, args.causal)
     q_h, k_h, v_h = xsgen.workload_inputs(args.workload)
-    as_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(dev)
+    if args.q8:  # the same draws rounded to E4M3
+        q_h, k_h = e4m3_inputs(q_h), e4m3_inputs(k_h)
+    as_dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
     q, k, v = as_dev(q_h), as_dev(k_h), as_dev(v_h)
+    qk_bytes = nbytes // 2 if args.q8 else nbytes
     out = torch.empty(nbytes // 2, dtype=torch.int16, device=dev)
     head = torch.empty_like(out)
     serial = torch.empty_like(out)
@@ -278,7 +299,11 @@ def run_ours(args):
 
     # The timed call is the balanced-schedule fused call (the library's fastest
     # fused path); the whole-item call is timed beside it for reference.
-    if args.causal:  # causal attention runs the whole-item schedule only
+    if args.q8:
+        fused = lambda: xs.attn_a2a_q8(q, k, v, out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+        fused_whole = lambda: xs.attn_a2a_q8(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
+        attn = lambda: xs.attn_q8(q, k, v, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+    elif args.causal:  # causal attention runs the whole-item schedule only
         fused = lambda: xs.attn_causal_a2a(q, k, v, out, B, S, H, D, P, scale, stream=sptr)
         fused_whole = lambda: xs.attn_causal_a2a(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
         attn = lambda: xs.attn_causal(q, k, v, head, B, S, H, D, P, scale, stream=sptr)
@@ -298,6 +323,8 @@ def run_ours(args):
     # operand, attention, and the post-attention permute.
     if args.causal:
         uly_ok, uly_why = False, "the sequence-partitioned-load call is non-causal only"
+    elif args.q8:
+        uly_ok, uly_why = False, "the sequence-partitioned-load call takes bf16 q, k, v only"
     else:
         uly_ok = xs.ulysses_attn(q, k, v, out_whole, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr,
                                  check=False) == xs.XS_OK
@@ -370,7 +397,7 @@ def run_ours(args):
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
 
     # ---- end to end through the C ABI with host buffers
-    pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()
+    pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
     qh, kh, vh = pin(q_h), pin(k_h), pin(v_h)
     oh = torch.empty(out.numel(), dtype=torch.int16).pin_memory()
     e2e_ms = []
@@ -403,7 +430,13 @@ def run_ours(args):
     e_res = tfc_us - ta_us
     hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
-    traffic = recorded_traffic(w["name"] + (" causal" if args.causal else ""))
+    traffic = recorded_traffic(w["name"] + (" causal" if args.causal else "") + (" e4m3" if args.q8 else ""))
+    # Roofline peak: measured bf16 for bf16 inputs. With E4M3 q and k, the Q K^T
+    # half of the flops can run at the 8-bit rate (2x bf16, nominal ratio), so the
+    # peak for the call's mix is the harmonic combination 4/3 x bf16.
+    peak = peaks["bf16_tflops"] * (4.0 / 3.0 if args.q8 else 1.0)
+    peak_note = (f"{peak_src} bf16 dense (burst) x 4/3: Q K^T at the 8-bit rate (2x bf16, nominal ratio), P V bf16"
+                 if args.q8 else f"{peak_src} bf16 dense (burst)")
     if uly_ok:
         tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
         uly = {
@@ -420,14 +453,16 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3 q/k, bf16 v/p/o" if args.q8 else "bf16", "data": "synthetic",
         "config": {
             "workload": w["name"], "B": B, "S": S, "H": H, "D": D, "P": P, "scale": scale,
-            "inputs": "PCG32 -> Box-Muller -> bf16, seed 1000+workload index, streams q=1 k=2 v=3",
+            "inputs": ("PCG32 -> Box-Muller -> bf16, seed 1000+workload index, streams q=1 k=2 v=3"
+                       + ("; q and k rounded to E4M3" if args.q8 else "")),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write",
             "timing": "CUDA events on the launch stream around each launch; value = K * flop / sum of times",
-            "call": ("xs_attn_causal_a2a (causal, whole-item longest-first schedule)" if args.causal
+            "call": ("xs_attn_a2a_q8 (E4M3 q and k, balanced schedule, caller-allocated workspace)" if args.q8
+                     else "xs_attn_causal_a2a (causal, whole-item longest-first schedule)" if args.causal
                      else "xs_attn_a2a_ws (balanced schedule, caller-allocated workspace)"),
             "mask": "causal" if args.causal else "none",
         },
@@ -441,20 +476,24 @@ def run_ours(args):
         "permute": {"gbs": 2 * nbytes / (tp_us * 1e-6) / 1e9, "frac_hbm": 2 * nbytes / (tp_us * 1e-6) / 1e9 /
                     peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
         "roofline": {"bound": "tensor",
-                     "kernel": ("attn_fwd_kernel<D, scatter, causal>" if args.causal
+                     "kernel": ("attn_fwd_kernel<D, scatter, E4M3 q/k> (balanced schedule)" if args.q8
+                                else "attn_fwd_kernel<D, scatter, causal>" if args.causal
                                 else "attn_fwd_kernel<D, scatter> (balanced schedule)"),
                      "achieved": kernel_tflops,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
-                     "peak_source": f"{peak_src} bf16 dense (burst)", "traffic": traffic,
-                     "algorithmic_flop_per_launch": flops, "algorithmic_min_bytes_per_launch": 4 * nbytes},
+                     "peak": peak, "unit": "TFLOP/s", "frac": kernel_tflops / peak,
+                     "peak_source": peak_note, "traffic": traffic,
+                     "algorithmic_flop_per_launch": flops,
+                     "algorithmic_min_bytes_per_launch": 2 * qk_bytes + 2 * nbytes},
         "ulysses": uly,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * qk_bytes + nbytes,
+                "d2h_bytes_per_step": nbytes,
                 "ms_per_step": e2e_max / args.steps},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world >= 1:
-        rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds, causal=args.causal)
+        rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds, causal=args.causal,
+                                                     q8=args.q8)
         line["cpu_baseline"] = {
             "value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{rows} uniformly drawn query rows of this workload in {wall:.1f} s wall (4*S*D flop per row)"}
@@ -475,11 +514,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--causal", action="store_true",
                     help="time causal attention (query i sees keys 0..i) instead of full attention")
+    ap.add_argument("--q8", action="store_true",
+                    help="time the E4M3 query/key call (D = 128 workloads; v and the output stay bf16)")
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="oracle seconds per step for --impl reference (default: sized to the run)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.q8 and args.causal:
+        ap.error("--q8 and --causal cannot be combined")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -121,19 +121,23 @@ xs_status get_encoder(EncodeTiledFn *fn) {
     return XS_OK;
 }
 
-// Tensor map over a head-partitioned tensor [P*B][S][Hl][D] (bf16), box = 64
-// columns x 128 tokens of one head, 128-byte swizzle (the tcgen05 K-major /
-// MN-major operand layout with 128-byte rows).
-xs_status make_head_map(CUtensorMap *m, const void *ptr, int B, int S, int H, int D, int P, const char *name) {
+// Tensor map over a head-partitioned tensor [P*B][S][Hl][D] of bf16 (esize 2)
+// or E4M3 bytes (esize 1), box = 128 bytes of columns x 128 tokens of one
+// head, 128-byte swizzle (the tcgen05 K-major / MN-major operand layout with
+// 128-byte rows).
+xs_status make_head_map(CUtensorMap *m, const void *ptr, int B, int S, int H, int D, int P, const char *name,
+                        int esize = 2) {
     EncodeTiledFn enc;
     xs_status st = get_encoder(&enc);
     if (st) return st;
     const int Hl = H / P;
+    const cuuint64_t e = (cuuint64_t)esize;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hl, (cuuint64_t)S, (cuuint64_t)P * (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hl * D * 2, (cuuint64_t)S * Hl * D * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * e, (cuuint64_t)Hl * D * e, (cuuint64_t)S * Hl * D * e};
+    const cuuint32_t box[4] = {(cuuint32_t)(128 / esize), 1, 128, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+    CUresult r = enc(m, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void *>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(XS_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
@@ -174,16 +178,34 @@ int gcd_int(int a, int b) {
 
 std::atomic<uint32_t> g_generation{1};
 
+// What an attention call does besides the plain head-partitioned one.
+struct CallOpts {
+    int epi = 0;              // 0: head-partitioned output; 1: All-to-All scatter
+    void *ws = nullptr;       // balanced-schedule workspace (NULL: whole-item schedule)
+    size_t ws_bytes = 0;
+    int layout = 0;           // 1: q, k, v and out sequence-partitioned (epi must be 1)
+    void *trace = nullptr;    // epilogue trace buffer
+    size_t trace_bytes = 0;
+    bool causal = false;
+    bool q8 = false;          // q and k hold E4M3 bytes (D = 128, layout 0)
+};
+
 // layout 0: q, k, v head-partitioned, out as `epi` says. layout 1: q, k, v and
 // out sequence-partitioned (both All-to-Alls fused; `epi` must be 1).
 xs_status attention_call(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
-                         float scale, void *stream, int epi, void *ws = nullptr, size_t ws_bytes = 0, int layout = 0,
-                         void *trace = nullptr, size_t trace_bytes = 0, bool causal = false) {
+                         float scale, void *stream, const CallOpts &o) {
+    const int epi = o.epi, layout = o.layout;
+    void *const ws = o.ws, *const trace = o.trace;
+    const size_t ws_bytes = o.ws_bytes, trace_bytes = o.trace_bytes;
+    const bool causal = o.causal;
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(XS_ERR_SHAPE, "scale must be positive and finite");
+    if (o.q8 && D != 128)
+        return fail(XS_ERR_UNSUPPORTED, "E4M3 queries and keys are built for D=128 only (got D=%d)", D);
+    const size_t qk_bytes = o.q8 ? bytes / 2 : bytes;
     if (trace) {
         if (D != 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing is built for D=128 only (got D=%d)", D);
         if (S % 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing needs S a multiple of 128 (got S=%d)", S);
@@ -195,12 +217,12 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     }
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return fail(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
-    if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
+    if (overlaps(out, bytes, q, qk_bytes) || overlaps(out, bytes, k, qk_bytes) || overlaps(out, bytes, v, bytes))
         return fail(XS_ERR_ALIAS, "out overlaps q, k or v");
     if (!ws && ws_bytes) return fail(XS_ERR_WORKSPACE, "workspace is NULL but workspace_bytes is %zu", ws_bytes);
     if (ws) {
         if (((uintptr_t)ws & 255u) != 0) return fail(XS_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-        if (overlaps(ws, ws_bytes, q, bytes) || overlaps(ws, ws_bytes, k, bytes) || overlaps(ws, ws_bytes, v, bytes) ||
+        if (overlaps(ws, ws_bytes, q, qk_bytes) || overlaps(ws, ws_bytes, k, qk_bytes) || overlaps(ws, ws_bytes, v, bytes) ||
             overlaps(ws, ws_bytes, out, bytes))
             return fail(XS_ERR_WORKSPACE, "workspace overlaps q, k, v or out");
     }
@@ -218,8 +240,8 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     xs::OperandMaps<1> head_maps;
     xs::OperandMaps<xs::kMaxRanks> rank_maps;
     if (layout == 0) {
-        if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q")) ||
-            (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k")) ||
+        if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q", o.q8 ? 1 : 2)) ||
+            (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k", o.q8 ? 1 : 2)) ||
             (st = make_head_map(&head_maps.v[0], v, B, S, H, D, P, "v")))
             return st;
     } else {
@@ -277,8 +299,9 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         if (e != cudaSuccess) return fail_cuda("traced attention launch", e);
         return XS_OK;
     }
-    cudaError_t e = layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
-                                : xs::launch_ulysses(D, rank_maps, p, grid, s);
+    cudaError_t e = o.q8          ? xs::launch_attention_q8_d128(epi, head_maps, p, grid, s)
+                    : layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
+                                  : xs::launch_ulysses(D, rank_maps, p, grid, s);
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
     return XS_OK;
 }
@@ -295,43 +318,85 @@ extern "C" {
 
 xs_status xs_attn_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                       float scale, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1);
+    CallOpts o;
+    o.epi = 1;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                   float scale, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0);
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, CallOpts());
 }
 
 xs_status xs_attn_a2a_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                          float scale, void *workspace, size_t workspace_bytes, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes);
+    CallOpts o;
+    o.epi = 1;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_ws(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                      float scale, void *workspace, size_t workspace_bytes, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0, workspace, workspace_bytes);
+    CallOpts o;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_ulysses_attn(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                           float scale, void *workspace, size_t workspace_bytes, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, workspace, workspace_bytes, 1);
+    CallOpts o;
+    o.epi = 1;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.layout = 1;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_causal_a2a(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
                              int P, float scale, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, nullptr, 0, 0, nullptr, 0, true);
+    CallOpts o;
+    o.epi = 1;
+    o.causal = true;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_causal(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D, int P,
                          float scale, void *stream) {
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 0, nullptr, 0, 0, nullptr, 0, true);
+    CallOpts o;
+    o.causal = true;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_a2a_q8(const void *q8, const void *k8, const void *v, void *out, int B, int S, int H, int D, int P,
+                         float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.epi = 1;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.q8 = true;
+    return attention_call(q8, k8, v, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_q8(const void *q8, const void *k8, const void *v, void *out, int B, int S, int H, int D, int P,
+                     float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.q8 = true;
+    return attention_call(q8, k8, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,
                             int P, float scale, void *trace, size_t trace_bytes, void *stream) {
     if (!trace) return fail(XS_ERR_NULL, "trace must be non-NULL");
-    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, 1, nullptr, 0, 0, trace, trace_bytes);
+    CallOpts o;
+    o.epi = 1;
+    o.trace = trace;
+    o.trace_bytes = trace_bytes;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_trace_layout(int B, int S, int H, int D, int P, int *ctas, int *items_per_cta, size_t *bytes) {

@@ -94,16 +94,20 @@ __device__ __forceinline__ bool warp_bwait(uint32_t bar, uint32_t parity, volati
 }
 
 
-template <int D> struct Cfg {
+// Q8: Q and K are E4M3 bytes (one 128-byte swizzle block per row at D = 128);
+// V, P and the output stay bf16.
+template <int D, bool Q8 = false> struct Cfg {
     static_assert(D == 64 || D == 96 || D == 128, "head dimension");
+    static_assert(!Q8 || D == 128, "E4M3 queries and keys are built for D = 128");
     // 64-column (128-byte) swizzle blocks per row; with D = 96 the second block
     // is half used (TMA zero-fills its other half)
     static constexpr int kNDB = (D + 63) / 64;
     static constexpr uint32_t kBlk = 128u * 128u;       // one swizzle block of a 128-row tile
-    static constexpr uint32_t kTile = kNDB * kBlk;      // a 128-row Q, K or V tile in shared memory
+    static constexpr uint32_t kTile = kNDB * kBlk;      // a 128-row bf16 tile in shared memory
+    static constexpr uint32_t kQKTile = Q8 ? 128u * D : kTile;  // a 128-row Q or K tile
     static constexpr int kSlots = 4;                    // K/V ring slots (K and V alternate)
     static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffKV = kOffQ + 2 * kTile;
+    static constexpr uint32_t kOffKV = kOffQ + 2 * kQKTile;
     static constexpr uint32_t kOffStage = kOffKV + kSlots * kTile;
     static constexpr uint32_t kStageWarp = 32u * 128u;  // 32 rows x 64 bf16 per epilogue warp
     static constexpr uint32_t kOffBar = kOffStage + 4 * kStageWarp;
@@ -503,10 +507,11 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU, bool Q8 = false>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, Q8>;
+    static_assert(!Q8 || LD == 0, "E4M3 inputs are head-partitioned");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -588,13 +593,15 @@ __global__ void __launch_bounds__(512, 1)
                 for (int t = 0; t < 2 && ok; ++t) {
                     ok = bwait(BAR(BQ_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteLoadQ);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kTile);
+                    mbar_arrive_expect_tx(BAR(BQ_FULL + t), C::kQKTile);
                     const int s0 = (2 * w.pair + t) * 128;  // past S for an absent tile: zero fill
                     if (TRACE && it == 0 && t == 0) cta_times[2] = globaltimer_ns();
                     if (LD) {
                         int rs, sl;
                         seq_position(p, s0, rs, sl);
                         load_rows_seq<D>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), p, b, h, rs, sl);
+                    } else if (Q8) {  // one 128-byte box per row: 128 E4M3 elements
+                        tma_load_4d(sQ + t * C::kQKTile, tm.q, BAR(BQ_FULL + t), 0, w.hl, s0, w.rb);
                     } else {
                         load_rows_head<D>(sQ + t * C::kTile, tm.q, BAR(BQ_FULL + t), w.rb, w.hl, s0);
                     }
@@ -606,9 +613,11 @@ __global__ void __launch_bounds__(512, 1)
                         const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u;
                         ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(BAR(BKV_FULL + slot), C::kTile);
+                        mbar_arrive_expect_tx(BAR(BKV_FULL + slot), kv ? C::kTile : C::kQKTile);
                         const CUtensorMap *m = kv ? tm.v : tm.k;
-                        if (LD)
+                        if (Q8 && !kv)
+                            tma_load_4d(sKV + slot * C::kTile, m, BAR(BKV_FULL + slot), 0, w.hl, j * 128, w.rb);
+                        else if (LD)
                             load_rows_seq<D>(sKV + slot * C::kTile, m, BAR(BKV_FULL + slot), p, b, h, rs, sl);
                         else
                             load_rows_head<D>(sKV + slot * C::kTile, m, BAR(BKV_FULL + slot), w.rb, w.hl, j * 128);
@@ -629,20 +638,24 @@ __global__ void __launch_bounds__(512, 1)
             }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
+            constexpr uint32_t idS = Q8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, 0);
             constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
             // Descriptors differ only in the start-address field (address >> 4 in
             // the low 14 bits), so each MMA adds a compile-time offset to a base.
             const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
             const uint64_t dV = sdesc_sw128(0, C::kBlk, 1024);  // MN-major V, 64-column blocks kBlk apart
             auto issue_S = [&](int t, uint32_t slot) {
-                const uint64_t qa = dK + (opaque(sQ + t * C::kTile) >> 4);
+                const uint64_t qa = dK + (opaque(sQ + t * C::kQKTile) >> 4);
                 const uint64_t ka = dK + (opaque(sKV + slot * C::kTile) >> 4);
                 const uint32_t d = opaque(tmem + C::colS(t));
+                // one MMA per 32 bytes of a row: K = 16 bf16 or K = 32 E4M3 elements
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < (Q8 ? D / 32 : D / 16); ++kk) {
                     const uint32_t off = ((kk >> 2) * C::kBlk + (kk & 3) * 32) >> 4;
-                    tc_mma_ss(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
+                    if (Q8)
+                        tc_mma_ss_f8(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
+                    else
+                        tc_mma_ss(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t (+)= P_t V for K/V rows [16*k0, 16*k1) of the tile
@@ -870,7 +883,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
                 const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row);
-                const uint32_t stage = sQ + t * C::kTile + (warp & 3) * C::kStageWarp;
+                const uint32_t stage = sQ + t * C::kQKTile + (warp & 3) * C::kStageWarp;
                 const uint32_t pend = finish_piece<D, D % 64 ? 32 : 64, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
                                                           l, tO, dst, valid, [] {});
                 if (pend) {
@@ -1005,10 +1018,11 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false, bool Q8 = false>
 static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU>;
+    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU, Q8>;
+    using CQ = Cfg<D, Q8>;
     // The shared-memory limit is raised once per device and instance: setting a
     // function attribute before every launch makes each launch start much later.
     static std::atomic<uint64_t> configured{0};
@@ -1017,20 +1031,20 @@ static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
     if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::kSmemAlloc);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CQ::kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
+    kern<<<grid, 512, CQ::kSmemAlloc, stream>>>(maps, p);
     e = cudaGetLastError();
     if (e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources) {
         // the attribute was lost (for instance by a device reset): set it again once
         configured.fetch_and(~bit, std::memory_order_acq_rel);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)Cfg<D>::kSmemAlloc)) != cudaSuccess)
+                                      (int)CQ::kSmemAlloc)) != cudaSuccess)
             return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
-        kern<<<grid, 512, Cfg<D>::kSmemAlloc, stream>>>(maps, p);
+        kern<<<grid, 512, CQ::kSmemAlloc, stream>>>(maps, p);
         e = cudaGetLastError();
     }
     return e;

@@ -102,6 +102,9 @@ XS_DECLARE_ATTN_ENTRY(128)
 XS_DECLARE_ATTN_ENTRY(256)
 cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                          cudaStream_t stream);
+// E4M3 queries and keys (maps q, k over bytes), bf16 values; D = 128 only.
+cudaError_t launch_attention_q8_d128(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+                                     cudaStream_t stream);
 
 // Sets the calling thread's xs_last_error() text; returns `status`.
 int report_error(int status, const char *message);

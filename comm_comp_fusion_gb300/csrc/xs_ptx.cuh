@@ -116,6 +116,17 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (8-bit A and B, fp32 accumulate;
+// each MMA covers K = 32 elements, 32 bytes of a row).
+__device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Same, with the A operand read from tensor memory.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -147,6 +158,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
            | (1u << 7)                            // A format: BF16
            | (1u << 10)                           // B format: BF16
            | ((uint32_t)b_mn_major << 16)         // B major-ness
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, fp32 accumulator, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                              // D format: F32
+           | (0u << 7) | (0u << 10)               // A, B format: E4M3
            | ((uint32_t)(N >> 3) << 17)           // N / 8
            | ((uint32_t)(M >> 4) << 24);          // M / 16
 }

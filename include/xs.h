@@ -40,7 +40,7 @@
  *     non-zero xs_status, enqueues nothing and leaves `out` untouched;
  *     xs_last_error() then describes it.
  *   - Shapes: B >= 0, S >= 0 (B == 0 or S == 0 is a valid empty call that
- *     enqueues nothing), H >= 1, P >= 1, H % P == 0, S % P == 0, D in {64, 128},
+ *     enqueues nothing), H >= 1, P >= 1, H % P == 0, S % P == 0, D in {64, 96, 128, 256},
  *     scale positive and finite. Every tensor must stay below 2^40 bytes. S need
  *     not be a multiple of 128: the last query tile is then partial (rows past
  *     S are neither computed into nor stored) and the keys past S in the last
@@ -67,7 +67,7 @@ typedef enum {
     XS_ERR_NULL = 1,        /* a required pointer is NULL */
     XS_ERR_SHAPE = 2,       /* a shape rule above is violated */
     XS_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
-    XS_ERR_UNSUPPORTED = 4, /* D not in {64,128}, wrong GPU, or a pointer that is not device memory */
+    XS_ERR_UNSUPPORTED = 4, /* D not in {64,96,128,256}, wrong GPU, or a pointer that is not device memory */
     XS_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed (message in xs_last_error) */
     XS_ERR_TIMEOUT = 6,     /* a bounded in-kernel wait ran out (reported by xs_device_status) */
     XS_ERR_ALIAS = 7,       /* out overlaps an input */
@@ -200,6 +200,31 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
  */
 xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const void *v, void *out, int B, int S, int H,
                               int D, int P, float scale, void *stream);
+
+/*
+ * Fused attention + All-to-All scatter with 8-bit queries and keys: an
+ * extension, the X-Stage paper evaluates bf16 only. Same operation as
+ * xs_attn_a2a_ws / xs_attn_ws, with Q K^T taken from E4M3 inputs.
+ *   q8, k8 : head-partitioned [P][B][S][Hl][D] bytes, each one OCP OFP8 E4M3
+ *            value (sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ *            infinities; 0x7F and 0xFF are NaN). Read only.
+ *   v      : head-partitioned [P][B][S][Hl][D] bf16, read only.
+ *   out    : bf16, sequence-partitioned [P][B][Sl][H][D] (xs_attn_a2a_q8) or
+ *            head-partitioned like v (xs_attn_q8), fully overwritten.
+ *   scale  : multiplies the exact product of the decoded q8 and k8 before the
+ *            softmax; per-tensor dequantisation factors of q8 and k8 fold in
+ *            here (softmax scale x q factor x k factor). > 0.
+ *   workspace, workspace_bytes : as for xs_attn_a2a_ws (the same size;
+ *            NULL, 0: whole-item schedule).
+ * D = 128 only (XS_ERR_UNSUPPORTED otherwise). Q K^T runs on the 8-bit tensor
+ * path with fp32 accumulation; the softmax, P and P V stay as in the bf16
+ * calls. xs_attn_a2a_q8 is bit-identical to xs_a2a_permute(xs_attn_q8(...)).
+ * XS_ERR_ALIAS when out overlaps the B*S*H*D bytes of q8 or k8 or the bf16 v.
+ */
+xs_status xs_attn_a2a_q8(const void *q8, const void *k8, const void *v, void *out, int B, int S, int H, int D,
+                         int P, float scale, void *workspace, size_t workspace_bytes, void *stream);
+xs_status xs_attn_q8(const void *q8, const void *k8, const void *v, void *out, int B, int S, int H, int D, int P,
+                     float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * The fused call (xs_attn_a2a, whole-item schedule) with its epilogue traced:

@@ -152,3 +152,27 @@ def test_valid_call_without_gpu_fails_loudly(xs):
     assert xs.last_error()
     with pytest.raises(xs.XsError):
         xs.attn_a2a(Q, K, V, O, 1, 256, 8, 64, 4, 0.125)
+
+
+def test_q8_argument_checks(xs):
+    W = 0x50000000
+    f = lambda q=Q, k=K, o=O, ws=None, nb=0, **kw: getattr(xs, kw.pop("fn", "attn_a2a_q8"))(
+        q, k, V, o, kw.get("B", 1), kw.get("S", 256), kw.get("H", 8), kw.get("D", 128), kw.get("P", 4),
+        kw.get("scale", 0.088), ws, nb, check=False)
+    for fn in ("attn_a2a_q8", "attn_q8"):
+        assert f(fn=fn, D=64) == xs.XS_ERR_UNSUPPORTED and "D=128" in xs.last_error()
+        assert f(fn=fn, D=256) == xs.XS_ERR_UNSUPPORTED
+        assert f(fn=fn, q=0) == xs.XS_ERR_NULL
+        assert f(fn=fn, k=K + 8) == xs.XS_ERR_ALIGN
+        assert f(fn=fn, scale=0.0) == xs.XS_ERR_SHAPE
+        assert f(fn=fn, ws=None, nb=64) == xs.XS_ERR_WORKSPACE
+        assert f(fn=fn, B=0) == xs.XS_OK
+    # q8 and k8 hold one byte per element: B*S*H*D = 262144 bytes here
+    assert f(o=Q + 262144 - 16) == xs.XS_ERR_ALIAS
+    assert f(o=K + 262144 - 16) == xs.XS_ERR_ALIAS
+    assert f(o=V + 524288 - 16) == xs.XS_ERR_ALIAS
+    assert f(ws=W, nb=1 << 20, k=W + (1 << 20) - 256) == xs.XS_ERR_WORKSPACE
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        # past the end of q8: only the missing GPU stops the call
+        assert f(o=Q + 262144) in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
