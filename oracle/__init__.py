@@ -64,9 +64,10 @@ def _load():
         lib.xs_oracle_attention_a2a_ex.restype = ci
         lib.xs_oracle_e4m3_decode.argtypes = [vp, vp, i64]
         lib.xs_oracle_e4m3_decode.restype = ci
-        lib.xs_oracle_attention_q8.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
+        lib.xs_oracle_attention_q8.argtypes = [vp, vp, vp, ci, vp, i64, i64, i64, i64, i64, dbl, ci, ci]
         lib.xs_oracle_attention_q8.restype = ci
-        lib.xs_oracle_attention_rows_q8.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, ci, vp, i64, vp, ci]
+        lib.xs_oracle_attention_rows_q8.argtypes = [vp, vp, vp, ci, i64, i64, i64, i64, i64, dbl, ci, vp, i64, vp,
+                                                    ci]
         lib.xs_oracle_attention_rows_q8.restype = ci
         lib.xs_oracle_a2a.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64]
         lib.xs_oracle_a2a.restype = ctypes.c_int
@@ -145,21 +146,31 @@ def e4m3_decode(codes):
     return out
 
 
+def _v_any(v):
+    """v as bf16 bit patterns (uint16) or, when given as uint8, E4M3 bytes; -> (array, is_e4m3)."""
+    v = np.asarray(v)
+    return (_u8(v), 1) if v.dtype == np.uint8 else (_u16(v), 0)
+
+
 def attention_q8(q8, k8, v, B, S, H, D, P, scale, causal=False, nthreads=0):
-    """Head-partitioned fp64 attention with q and k given as E4M3 bytes, v bf16."""
-    q8, k8, v = _u8(q8), _u8(k8), _u16(v)
+    """Head-partitioned fp64 attention with q and k given as E4M3 bytes; v is bf16
+    (uint16 bit patterns) or E4M3 (uint8 bytes)."""
+    q8, k8 = _u8(q8), _u8(k8)
+    v, v8 = _v_any(v)
     out = np.empty((P, B, S, H // P, D), dtype=np.float64)
-    _check(_load().xs_oracle_attention_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, out.ctypes.data,
+    _check(_load().xs_oracle_attention_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, v8, out.ctypes.data,
                                           B, S, H, D, P, float(scale), int(causal), nthreads))
     return out
 
 
 def attention_rows_q8(q8, k8, v, B, S, H, D, P, scale, rows, causal=False, nthreads=0):
-    """fp64 attention with E4M3 q and k for selected head-partitioned rows -> [n][D]."""
-    q8, k8, v = _u8(q8), _u8(k8), _u16(v)
+    """fp64 attention with E4M3 q and k (v bf16 or E4M3, as for attention_q8) for
+    selected head-partitioned rows -> [n][D]."""
+    q8, k8 = _u8(q8), _u8(k8)
+    v, v8 = _v_any(v)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     out = np.empty((rows.size, D), dtype=np.float64)
-    _check(_load().xs_oracle_attention_rows_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, B, S, H, D, P,
+    _check(_load().xs_oracle_attention_rows_q8(q8.ctypes.data, k8.ctypes.data, v.ctypes.data, v8, B, S, H, D, P,
                                                float(scale), int(causal), rows.ctypes.data, rows.size,
                                                out.ctypes.data, nthreads))
     return out

@@ -23,8 +23,8 @@
  *    out). Reading taken: query token i of a head sees key tokens j <= i of the
  *    same sequence, so every sum above runs over j = 0..i instead of 0..S-1.
  *
- *  - FP8 query/key inputs (an extension; the pages evaluate bf16 only): q and k
- *    may be given as E4M3 bytes, the format of the OCP 8-bit floating point
+ *  - FP8 inputs (an extension; the pages evaluate bf16 only): q and k, and
+ *    optionally v, may be given as E4M3 bytes, the format of the OCP 8-bit floating point
  *    specification (OFP8): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
  *    bits; exponent field 0 holds subnormals m/8 * 2^-6; S.1111.111 is NaN and
  *    there is no infinity (largest finite 1.75 * 2^8 = 448). They are widened
@@ -162,6 +162,7 @@ int xs_oracle_a2a_inverse(const void *in, void *out, int64_t B, int64_t S, int64
 typedef struct {
     const uint16_t *q, *k, *v;
     const uint8_t *q8, *k8;  /* E4M3 q and k instead of q and k when not NULL */
+    const uint8_t *v8;       /* E4M3 v instead of v when not NULL */
     int64_t B, S, H, D, P;
     double scale;
     int causal;        /* 1: query token i sees keys 0..i only */
@@ -215,8 +216,13 @@ static void attend_row(const attn_job_t *j, int64_t row, double *p, double *qi, 
     /* o = sum_j p_j v_j / l ; for every d the sum runs over j in ascending order */
     for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
     for (int64_t t = t0; t < t1; ++t) {
-        const uint16_t *vt = j->v + head_base + t * row_stride;
-        for (int64_t d = 0; d < D; ++d) o[d] += p[t] * bf16_to_double(vt[d]);
+        if (j->v8) {
+            const uint8_t *vt = j->v8 + head_base + t * row_stride;
+            for (int64_t d = 0; d < D; ++d) o[d] += p[t] * e4m3_to_double(vt[d]);
+        } else {
+            const uint16_t *vt = j->v + head_base + t * row_stride;
+            for (int64_t d = 0; d < D; ++d) o[d] += p[t] * bf16_to_double(vt[d]);
+        }
     }
     for (int64_t d = 0; d < D; ++d) o[d] /= l;
 }
@@ -280,18 +286,20 @@ int xs_oracle_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t 
     int64_t total = P * B * S * (H / P);
     if (total == 0) return 1;
     if (!q || !k || !v || !o) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, 0, 0, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
+    attn_job_t base = {q, k, v, 0, 0, 0, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
     return run_attention(base, total, nthreads);
 }
 
-/* As xs_oracle_attention_ex with q and k given as E4M3 bytes (same layout). */
-int xs_oracle_attention_q8(const uint8_t *q8, const uint8_t *k8, const uint16_t *v, double *o, int64_t B, int64_t S,
-                           int64_t H, int64_t D, int64_t P, double scale, int causal, int nthreads) {
+/* As xs_oracle_attention_ex with q and k given as E4M3 bytes (same layout);
+ * v is bf16, or E4M3 bytes when v_e4m3 != 0. */
+int xs_oracle_attention_q8(const uint8_t *q8, const uint8_t *k8, const void *v, int v_e4m3, double *o, int64_t B,
+                           int64_t S, int64_t H, int64_t D, int64_t P, double scale, int causal, int nthreads) {
     if (check_shape(B, S, H, D, P)) return XSO_EINVAL;
     int64_t total = P * B * S * (H / P);
     if (total == 0) return 1;
     if (!q8 || !k8 || !v || !o) return XSO_EINVAL;
-    attn_job_t base = {0, 0, v, q8, k8, B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
+    attn_job_t base = {0, 0, v_e4m3 ? 0 : (const uint16_t *)v, q8, k8, v_e4m3 ? (const uint8_t *)v : 0,
+                       B, S, H, D, P, scale, causal != 0, 0, 0, o, 0, 0, 0};
     return run_attention(base, total, nthreads);
 }
 
@@ -310,20 +318,21 @@ int xs_oracle_attention_rows_ex(const uint16_t *q, const uint16_t *k, const uint
     int64_t total_rows = P * B * S * (H / P);
     for (int64_t i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total_rows) return XSO_EINVAL;
-    attn_job_t base = {q, k, v, 0, 0, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
+    attn_job_t base = {q, k, v, 0, 0, 0, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
     return run_attention(base, nrows, nthreads);
 }
 
-int xs_oracle_attention_rows_q8(const uint8_t *q8, const uint8_t *k8, const uint16_t *v, int64_t B, int64_t S,
-                                int64_t H, int64_t D, int64_t P, double scale, int causal, const int64_t *rows,
-                                int64_t nrows, double *o_rows, int nthreads) {
+int xs_oracle_attention_rows_q8(const uint8_t *q8, const uint8_t *k8, const void *v, int v_e4m3, int64_t B,
+                                int64_t S, int64_t H, int64_t D, int64_t P, double scale, int causal,
+                                const int64_t *rows, int64_t nrows, double *o_rows, int nthreads) {
     if (check_shape(B, S, H, D, P) || nrows < 0) return XSO_EINVAL;
     if (nrows == 0) return 1;
     if (!q8 || !k8 || !v || !rows || !o_rows) return XSO_EINVAL;
     int64_t total_rows = P * B * S * (H / P);
     for (int64_t i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total_rows) return XSO_EINVAL;
-    attn_job_t base = {0, 0, v, q8, k8, B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
+    attn_job_t base = {0, 0, v_e4m3 ? 0 : (const uint16_t *)v, q8, k8, v_e4m3 ? (const uint8_t *)v : 0,
+                       B, S, H, D, P, scale, causal != 0, rows, nrows, o_rows, 0, 0, 0};
     return run_attention(base, nrows, nthreads);
 }
 

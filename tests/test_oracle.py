@@ -206,6 +206,42 @@ def test_attention_q8_equals_bf16_on_widened_inputs():
                                   oracle.attention(widen(q8), widen(k8), v, B, S, H, D, P, 0.3).reshape(-1, D)[rows])
 
 
+def test_attention_e4m3_values_equal_bf16_on_widened_inputs():
+    """E4M3 v as well: still exactly the bf16 attention on the widened q, k, v."""
+    B, S, H, D, P = 2, 12, 4, 8, 2
+    shape = (P, B, S, H // P, D)
+    q8, k8, v8 = (xsgen.normal_e4m3(31, i, shape, s) for i, s in ((1, 2.0), (2, 2.0), (3, 24.0)))
+    widen = lambda c: xsgen.f32_to_bf16_bits(oracle.e4m3_decode(c).astype(np.float32))
+    assert (oracle.e4m3_decode(v8) < 0).any() and (np.abs(oracle.e4m3_decode(v8)) >= 64).any()
+    for causal in (False, True):
+        a = oracle.attention_q8(q8, k8, v8, B, S, H, D, P, 0.3, causal=causal)
+        b = oracle.attention(widen(q8), widen(k8), widen(v8), B, S, H, D, P, 0.3, causal=causal)
+        np.testing.assert_array_equal(a, b)
+    rows = np.array([0, 5, 41, P * B * S * (H // P) - 1])
+    np.testing.assert_array_equal(oracle.attention_rows_q8(q8, k8, v8, B, S, H, D, P, 0.3, rows, causal=True),
+                                  oracle.attention(widen(q8), widen(k8), widen(v8), B, S, H, D, P, 0.3,
+                                                   causal=True).reshape(-1, D)[rows])
+
+
+def test_attention_e4m3_values_special_cases():
+    """Hand-checkable E4M3 cases: equal keys give the plain mean of the decoded
+    values; one dominant key returns its value row (the largest code, 448, and
+    the smallest subnormal, 2^-9, among them)."""
+    B, S, H, D, P = 1, 4, 1, 2, 1
+    q8 = np.zeros((P, B, S, H, D), dtype=np.uint8)           # q = 0: uniform weights
+    k8 = np.full_like(q8, 0x38)                              # 1.0
+    v8 = np.array([0x7E, 0x01, 0xC0, 0x30], dtype=np.uint8)  # 448, 2^-9, -2.0, 0.5
+    v8 = np.stack([v8, v8[::-1]], axis=-1).reshape(P, B, S, H, D)
+    o = oracle.attention_q8(q8, k8, v8, B, S, H, D, P, 1.0)
+    want = (448.0 + 2.0 ** -9 - 2.0 + 0.5) / 4.0
+    np.testing.assert_allclose(o.reshape(S, D), np.full((S, D), want), rtol=0, atol=1e-13)
+    q8 = np.full_like(q8, 0x38)                              # q = 1
+    k8 = np.array([0x00, 0x00, 0x78, 0x00], dtype=np.uint8)  # key 2 = 256, the others 0
+    k8 = np.repeat(k8, D).reshape(P, B, S, H, D)
+    o = oracle.attention_q8(q8, k8, v8, B, S, H, D, P, 1.0)  # logits 512 vs 0: weight 1 - O(e^-512)
+    np.testing.assert_array_equal(o.reshape(S, D), np.tile([-2.0, 2.0 ** -9], (S, 1)))
+
+
 # ------------------------------------------------------------------ invariants
 
 def test_rows_are_probabilities():
@@ -357,6 +393,11 @@ _MUTANTS = {
     "e4m3 exponent bias": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "e4m3 subnormal scale": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
     "e4m3 mantissa width": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 16.0, e - 7);"),
+    "e4m3 value row index": ("const uint8_t *vt = j->v8 + head_base + t * row_stride;",
+                             "const uint8_t *vt = j->v8 + head_base + (S - 1 - t) * row_stride;"),
+    "e4m3 value weight": ("o[d] += p[t] * e4m3_to_double(vt[d]);", "o[d] += e4m3_to_double(vt[d]);"),
+    "e4m3 value read as key": ("o[d] += p[t] * e4m3_to_double(vt[d]);",
+                               "o[d] += p[t] * e4m3_to_double(j->k8[head_base + t * row_stride + d]);"),
 }
 
 
@@ -387,6 +428,17 @@ def _pins_pass(lib):
     lib.xs_oracle_e4m3_decode(codes.ctypes.data, dec.ctypes.data, codes.size)
     want = np.array([np.nan if x == "nan" else x for x in g8.values()])
     ok = bool(np.array_equal(np.isnan(dec), np.isnan(want)) and np.array_equal(dec[~np.isnan(want)], want[~np.isnan(want)]))
+    # E4M3 q, k, v against the bf16 path on the widened values (exact)
+    lib.xs_oracle_attention_q8.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, i64, i64, i64, i64, dbl,
+                                           ctypes.c_int, ctypes.c_int]
+    B, S, H, D, P = 2, 12, 4, 8, 2
+    sh = (P, B, S, H // P, D)
+    q8, k8, v8 = (xsgen.normal_e4m3(31, i, sh, s) for i, s in ((1, 2.0), (2, 2.0), (3, 24.0)))
+    wid = lambda c: xsgen.f32_to_bf16_bits(_decode_ref(c).astype(np.float32))
+    o8 = np.empty(sh)
+    lib.xs_oracle_attention_q8(q8.ctypes.data, k8.ctypes.data, v8.ctypes.data, 1, o8.ctypes.data,
+                               B, S, H, D, P, 0.3, 0, 2)
+    ok &= bool(np.array_equal(o8, attn(wid(q8), wid(k8), wid(v8), B, S, H, D, P, 0.3)))
     B, S, H, D, P, scale, sigma = TINY[3]
     q, k, v = xsgen.random_inputs(91 + S * 10 + D, P, B, S, H, D, sigma, 1.0)
     ok &= bool(np.allclose(attn_causal(q, k, v, B, S, H, D, P, scale),
@@ -417,6 +469,14 @@ def _pins_pass(lib):
     lib.xs_oracle_a2a(x.ctypes.data, y.ctypes.data, B, S, H, D, P, 4)
     ok &= bool(np.array_equal(y, np.array(a2a["out"], dtype=np.int32)))
     return ok
+
+
+def _decode_ref(codes):
+    """E4M3 decode by the generator's independent value table (not the oracle's)."""
+    vals = xsgen._e4m3_positive_values()
+    c = np.asarray(codes)
+    mag = vals[np.minimum(c & 0x7F, 0x7E)]
+    return np.where(c & 0x80, -mag, mag)
 
 
 def test_pins_catch_planted_mistakes(tmp_path):
