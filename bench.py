@@ -25,7 +25,8 @@ times the same call with the inputs copied in from pinned host memory and the
 output copied back inside the timed region.
 
 --q8 times the E4M3 query/key call (xs_attn_a2a_q8) on the same draws
-rounded to E4M3; v and the output stay bf16.
+rounded to E4M3; v and the output stay bf16. --qkv8 times the call with E4M3
+values as well (xs_attn_a2a_qkv8).
 
 --impl reference times the fp64 CPU oracle (the checker of this library, not
 a tuned CPU implementation) on the host cores over a bounded sample of query
@@ -229,6 +230,8 @@ def run_reference(args):
     q, k, v = xsgen.workload_inputs(args.workload)
     if args.q8:
         q, k = e4m3_inputs(q), e4m3_inputs(k)
+    if args.v8:
+        v = e4m3_inputs(v)
     # Each step is a bounded sample so that warm-up plus K steps stay within a few minutes.
     per_step = args.ref_step_seconds or max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
@@ -249,7 +252,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "S": w["S"], "H": w["H"], "D": w["D"], "P": w["P"],
                    "parallelism": "replicas", "mask": "causal" if args.causal else "none",
-                   "inputs": "q, k E4M3, v bf16" if args.q8 else "q, k, v bf16",
+                   "inputs": "q, k, v E4M3" if args.v8 else "q, k E4M3, v bf16" if args.q8 else "q, k, v bf16",
                    "what": "fp64 CPU oracle (two-pass softmax attention per row)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -284,9 +287,12 @@ def run_ours(args):
     q_h, k_h, v_h = xsgen.workload_inputs(args.workload)
     if args.q8:  # the same draws rounded to E4M3
         q_h, k_h = e4m3_inputs(q_h), e4m3_inputs(k_h)
+    if args.v8:
+        v_h = e4m3_inputs(v_h)
     as_dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
     q, k, v = as_dev(q_h), as_dev(k_h), as_dev(v_h)
     qk_bytes = nbytes // 2 if args.q8 else nbytes
+    v_bytes = nbytes // 2 if args.v8 else nbytes
     out = torch.empty(nbytes // 2, dtype=torch.int16, device=dev)
     head = torch.empty_like(out)
     serial = torch.empty_like(out)
@@ -299,7 +305,11 @@ def run_ours(args):
 
     # The timed call is the balanced-schedule fused call (the library's fastest
     # fused path); the whole-item call is timed beside it for reference.
-    if args.q8:
+    if args.v8:
+        fused = lambda: xs.attn_a2a_qkv8(q, k, v, out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+        fused_whole = lambda: xs.attn_a2a_qkv8(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
+        attn = lambda: xs.attn_qkv8(q, k, v, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
+    elif args.q8:
         fused = lambda: xs.attn_a2a_q8(q, k, v, out, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
         fused_whole = lambda: xs.attn_a2a_q8(q, k, v, out_whole, B, S, H, D, P, scale, stream=sptr)
         attn = lambda: xs.attn_q8(q, k, v, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
@@ -324,7 +334,7 @@ def run_ours(args):
     if args.causal:
         uly_ok, uly_why = False, "the sequence-partitioned-load call is non-causal only"
     elif args.q8:
-        uly_ok, uly_why = False, "the sequence-partitioned-load call takes bf16 q, k, v only"
+        uly_ok, uly_why = False, "the sequence-partitioned-load call takes bf16 q, k, v only"  # q8 and qkv8
     else:
         uly_ok = xs.ulysses_attn(q, k, v, out_whole, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr,
                                  check=False) == xs.XS_OK
@@ -430,12 +440,15 @@ def run_ours(args):
     e_res = tfc_us - ta_us
     hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
-    traffic = recorded_traffic(w["name"] + (" causal" if args.causal else "") + (" e4m3" if args.q8 else ""))
+    traffic = recorded_traffic(w["name"] + (" causal" if args.causal else "")
+                               + (" e4m3 qkv" if args.v8 else " e4m3" if args.q8 else ""))
     # Roofline peak: measured bf16 for bf16 inputs. With E4M3 q and k, the Q K^T
     # half of the flops can run at the 8-bit rate (2x bf16, nominal ratio), so the
-    # peak for the call's mix is the harmonic combination 4/3 x bf16.
+    # peak for the call's mix is the harmonic combination 4/3 x bf16 (P V runs
+    # as bf16, or as f16 with E4M3 values: the same rate).
     peak = peaks["bf16_tflops"] * (4.0 / 3.0 if args.q8 else 1.0)
-    peak_note = (f"{peak_src} bf16 dense (burst) x 4/3: Q K^T at the 8-bit rate (2x bf16, nominal ratio), P V bf16"
+    peak_note = (f"{peak_src} bf16 dense (burst) x 4/3: Q K^T at the 8-bit rate (2x bf16, nominal ratio), "
+                 f"P V at the 16-bit rate"
                  if args.q8 else f"{peak_src} bf16 dense (burst)")
     if uly_ok:
         tu_us, tuf_us, tus_us, ti_us = (1e3 * med(t) for t in (t_uly, t_uly_fused, t_uly_serial, t_inv))
@@ -453,15 +466,18 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 q/k, bf16 v/p/o" if args.q8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("e4m3 q/k/v, f16 p, bf16 o" if args.v8 else "e4m3 q/k, bf16 v/p/o" if args.q8 else "bf16"),
         "config": {
             "workload": w["name"], "B": B, "S": S, "H": H, "D": D, "P": P, "scale": scale,
             "inputs": ("PCG32 -> Box-Muller -> bf16, seed 1000+workload index, streams q=1 k=2 v=3"
-                       + ("; q and k rounded to E4M3" if args.q8 else "")),
+                       + ("; q, k and v rounded to E4M3" if args.v8 else "; q and k rounded to E4M3" if args.q8
+                          else "")),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write",
             "timing": "CUDA events on the launch stream around each launch; value = K * flop / sum of times",
-            "call": ("xs_attn_a2a_q8 (E4M3 q and k, balanced schedule, caller-allocated workspace)" if args.q8
+            "call": ("xs_attn_a2a_qkv8 (E4M3 q, k and v, balanced schedule, caller-allocated workspace)" if args.v8
+                     else "xs_attn_a2a_q8 (E4M3 q and k, balanced schedule, caller-allocated workspace)" if args.q8
                      else "xs_attn_causal_a2a (causal, whole-item longest-first schedule)" if args.causal
                      else "xs_attn_a2a_ws (balanced schedule, caller-allocated workspace)"),
             "mask": "causal" if args.causal else "none",
@@ -476,16 +492,17 @@ def run_ours(args):
         "permute": {"gbs": 2 * nbytes / (tp_us * 1e-6) / 1e9, "frac_hbm": 2 * nbytes / (tp_us * 1e-6) / 1e9 /
                     peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
         "roofline": {"bound": "tensor",
-                     "kernel": ("attn_fwd_kernel<D, scatter, E4M3 q/k> (balanced schedule)" if args.q8
+                     "kernel": ("attn_fwd_kernel<D, scatter, E4M3 q/k/v> (balanced schedule)" if args.v8
+                                else "attn_fwd_kernel<D, scatter, E4M3 q/k> (balanced schedule)" if args.q8
                                 else "attn_fwd_kernel<D, scatter, causal>" if args.causal
                                 else "attn_fwd_kernel<D, scatter> (balanced schedule)"),
                      "achieved": kernel_tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": kernel_tflops / peak,
                      "peak_source": peak_note, "traffic": traffic,
                      "algorithmic_flop_per_launch": flops,
-                     "algorithmic_min_bytes_per_launch": 2 * qk_bytes + 2 * nbytes},
+                     "algorithmic_min_bytes_per_launch": 2 * qk_bytes + v_bytes + nbytes},
         "ulysses": uly,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * qk_bytes + nbytes,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * qk_bytes + v_bytes,
                 "d2h_bytes_per_step": nbytes,
                 "ms_per_step": e2e_max / args.steps},
         "gpu_launches": gpu_launches,
@@ -516,13 +533,17 @@ def main(argv=None):
                     help="time causal attention (query i sees keys 0..i) instead of full attention")
     ap.add_argument("--q8", action="store_true",
                     help="time the E4M3 query/key call (D = 128 workloads; v and the output stay bf16)")
+    ap.add_argument("--qkv8", action="store_true",
+                    help="time the call with E4M3 queries, keys and values (D = 128 workloads)")
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="oracle seconds per step for --impl reference (default: sized to the run)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    args.v8 = args.qkv8
+    args.q8 = args.q8 or args.qkv8
     if args.q8 and args.causal:
-        ap.error("--q8 and --causal cannot be combined")
+        ap.error("--q8 / --qkv8 and --causal cannot be combined")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -40,6 +40,7 @@ EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_a2a_permute_inverse",
            "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size", "xs_attn_a2a_noalloc", "xs_last_error",
            "xs_device_status", "xs_selftest_wait_timeout", "xs_version", "xs_attn_a2a_trace", "xs_attn_trace_layout",
            "xs_attn_causal_a2a", "xs_attn_causal", "xs_attn_a2a_q8", "xs_attn_q8",
+           "xs_attn_a2a_qkv8", "xs_attn_qkv8",
            # include/xs_burst.h
            "xs_burst_rec_bytes", "xs_burst_gap")
 
@@ -93,6 +94,10 @@ def _load() -> ctypes.CDLL:
     lib.xs_attn_a2a_q8.restype = i
     lib.xs_attn_q8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_q8.restype = i
+    lib.xs_attn_a2a_qkv8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_a2a_qkv8.restype = i
+    lib.xs_attn_qkv8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_qkv8.restype = i
     lib.xs_attn_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(sz)]
     lib.xs_attn_workspace_size.restype = i
     lib.xs_attn_a2a_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
@@ -187,6 +192,21 @@ def attn_q8(q8, k8, v, out, B, S, H, D, P, scale, workspace=None, workspace_byte
     """Attention only with E4M3 queries and keys (``xs_attn_q8``), head-partitioned output."""
     st = lib.xs_attn_q8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
                         _nbytes(workspace, workspace_bytes), _stream(stream, v, out))
+    return _check(st) if check else st
+
+
+def attn_a2a_qkv8(q8, k8, v8, out, B, S, H, D, P, scale, workspace=None, workspace_bytes=None, stream=None,
+                  check=True):
+    """Fused call with E4M3 queries, keys and values (``xs_attn_a2a_qkv8``); bf16 output."""
+    st = lib.xs_attn_a2a_qkv8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                              _nbytes(workspace, workspace_bytes), _stream(stream, v8, out))
+    return _check(st) if check else st
+
+
+def attn_qkv8(q8, k8, v8, out, B, S, H, D, P, scale, workspace=None, workspace_bytes=None, stream=None, check=True):
+    """Attention only with E4M3 queries, keys and values (``xs_attn_qkv8``), head-partitioned output."""
+    st = lib.xs_attn_qkv8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                          _nbytes(workspace, workspace_bytes), _stream(stream, v8, out))
     return _check(st) if check else st
 
 

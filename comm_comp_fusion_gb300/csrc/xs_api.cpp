@@ -187,7 +187,7 @@ struct CallOpts {
     void *trace = nullptr;    // epilogue trace buffer
     size_t trace_bytes = 0;
     bool causal = false;
-    bool q8 = false;          // q and k hold E4M3 bytes (D = 128, layout 0)
+    int f8 = 0;               // 1: q and k hold E4M3 bytes; 2: q, k and v do (D = 128, layout 0)
 };
 
 // layout 0: q, k, v head-partitioned, out as `epi` says. layout 1: q, k, v and
@@ -203,9 +203,8 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(XS_ERR_SHAPE, "scale must be positive and finite");
-    if (o.q8 && D != 128)
-        return fail(XS_ERR_UNSUPPORTED, "E4M3 queries and keys are built for D=128 only (got D=%d)", D);
-    const size_t qk_bytes = o.q8 ? bytes / 2 : bytes;
+    if (o.f8 && D != 128) return fail(XS_ERR_UNSUPPORTED, "E4M3 inputs are built for D=128 only (got D=%d)", D);
+    const size_t qk_bytes = o.f8 ? bytes / 2 : bytes, v_bytes = o.f8 == 2 ? bytes / 2 : bytes;
     if (trace) {
         if (D != 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing is built for D=128 only (got D=%d)", D);
         if (S % 128) return fail(XS_ERR_UNSUPPORTED, "epilogue tracing needs S a multiple of 128 (got S=%d)", S);
@@ -217,12 +216,12 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     }
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return fail(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
-    if (overlaps(out, bytes, q, qk_bytes) || overlaps(out, bytes, k, qk_bytes) || overlaps(out, bytes, v, bytes))
+    if (overlaps(out, bytes, q, qk_bytes) || overlaps(out, bytes, k, qk_bytes) || overlaps(out, bytes, v, v_bytes))
         return fail(XS_ERR_ALIAS, "out overlaps q, k or v");
     if (!ws && ws_bytes) return fail(XS_ERR_WORKSPACE, "workspace is NULL but workspace_bytes is %zu", ws_bytes);
     if (ws) {
         if (((uintptr_t)ws & 255u) != 0) return fail(XS_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-        if (overlaps(ws, ws_bytes, q, qk_bytes) || overlaps(ws, ws_bytes, k, qk_bytes) || overlaps(ws, ws_bytes, v, bytes) ||
+        if (overlaps(ws, ws_bytes, q, qk_bytes) || overlaps(ws, ws_bytes, k, qk_bytes) || overlaps(ws, ws_bytes, v, v_bytes) ||
             overlaps(ws, ws_bytes, out, bytes))
             return fail(XS_ERR_WORKSPACE, "workspace overlaps q, k, v or out");
     }
@@ -240,9 +239,9 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     xs::OperandMaps<1> head_maps;
     xs::OperandMaps<xs::kMaxRanks> rank_maps;
     if (layout == 0) {
-        if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q", o.q8 ? 1 : 2)) ||
-            (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k", o.q8 ? 1 : 2)) ||
-            (st = make_head_map(&head_maps.v[0], v, B, S, H, D, P, "v")))
+        if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q", o.f8 ? 1 : 2)) ||
+            (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k", o.f8 ? 1 : 2)) ||
+            (st = make_head_map(&head_maps.v[0], v, B, S, H, D, P, "v", o.f8 == 2 ? 1 : 2)))
             return st;
     } else {
         memset(&rank_maps, 0, sizeof rank_maps);
@@ -299,7 +298,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         if (e != cudaSuccess) return fail_cuda("traced attention launch", e);
         return XS_OK;
     }
-    cudaError_t e = o.q8          ? xs::launch_attention_q8_d128(epi, head_maps, p, grid, s)
+    cudaError_t e = o.f8          ? xs::launch_attention_f8_d128(o.f8, epi, head_maps, p, grid, s)
                     : layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
                                   : xs::launch_ulysses(D, rank_maps, p, grid, s);
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
@@ -376,7 +375,7 @@ xs_status xs_attn_a2a_q8(const void *q8, const void *k8, const void *v, void *ou
     o.epi = 1;
     o.ws = workspace;
     o.ws_bytes = workspace_bytes;
-    o.q8 = true;
+    o.f8 = 1;
     return attention_call(q8, k8, v, out, B, S, H, D, P, scale, stream, o);
 }
 
@@ -385,8 +384,27 @@ xs_status xs_attn_q8(const void *q8, const void *k8, const void *v, void *out, i
     CallOpts o;
     o.ws = workspace;
     o.ws_bytes = workspace_bytes;
-    o.q8 = true;
+    o.f8 = 1;
     return attention_call(q8, k8, v, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_a2a_qkv8(const void *q8, const void *k8, const void *v8, void *out, int B, int S, int H, int D,
+                           int P, float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.epi = 1;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.f8 = 2;
+    return attention_call(q8, k8, v8, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out, int B, int S, int H, int D, int P,
+                       float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.f8 = 2;
+    return attention_call(q8, k8, v8, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,

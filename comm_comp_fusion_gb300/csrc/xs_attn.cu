@@ -117,7 +117,8 @@ cudaError_t read_device_error(unsigned int *value, bool clear, cudaStream_t stre
         if ((e = cudaMemcpyToSymbol(g_xs_error, &zero, sizeof(unsigned int))) != cudaSuccess) return e;
     }
     cudaError_t (*const per_d[])(unsigned int *, bool) = {read_error_word_d64, read_error_word_d96,
-                                                          read_error_word_d128, read_error_word_d256};
+                                                          read_error_word_d128, read_error_word_d256,
+                                                          read_error_word_f8};
     for (auto fn : per_d) {
         if ((e = fn(&w, clear)) != cudaSuccess) return e;
         all |= w;

@@ -1,6 +1,6 @@
 // xs_attn_d128.cu -- the attention kernel's instances for head dimension 128
 // (fused scatter and head-partitioned output, sequence-partitioned loads,
-// ragged and whole-tile sequence lengths, E4M3 queries and keys). The kernel itself is in
+// ragged and whole-tile sequence lengths). The kernel itself is in
 // xs_attn_kernel.cuh; one translation unit per head dimension keeps the build
 // parallel.
 #include "xs_attn_kernel.cuh"
@@ -12,16 +12,6 @@ XS_DEFINE_ATTN_ENTRY(128)
 cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                          cudaStream_t stream) {
     return launch_one<128, 1, 0, 1, false>(maps, p, grid, stream);
-}
-
-// E4M3 queries and keys, bf16 values: head-partitioned loads only.
-cudaError_t launch_attention_q8_d128(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
-                                     cudaStream_t stream) {
-    if (p.kv_tail < 128)
-        return epi ? launch_one<128, 1, 0, 0, true, false, true>(maps, p, grid, stream)
-                   : launch_one<128, 0, 0, 0, true, false, true>(maps, p, grid, stream);
-    return epi ? launch_one<128, 1, 0, 0, false, false, true>(maps, p, grid, stream)
-               : launch_one<128, 0, 0, 0, false, false, true>(maps, p, grid, stream);
 }
 
 }  // namespace xs

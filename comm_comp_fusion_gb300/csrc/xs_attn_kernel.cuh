@@ -94,11 +94,14 @@ __device__ __forceinline__ bool warp_bwait(uint32_t bar, uint32_t parity, volati
 }
 
 
-// Q8: Q and K are E4M3 bytes (one 128-byte swizzle block per row at D = 128);
-// V, P and the output stay bf16.
-template <int D, bool Q8 = false> struct Cfg {
+// F8 = 1: Q and K are E4M3 bytes (one 128-byte swizzle block per row at
+// D = 128); V, P and the output stay bf16. F8 = 2: V is E4M3 as well; it lands
+// in a two-slot staging ring and is widened exactly to f16 in its K/V ring
+// slot, and P is rounded to f16 for an f16 x f16 P V.
+template <int D, int F8 = 0> struct Cfg {
     static_assert(D == 64 || D == 96 || D == 128, "head dimension");
-    static_assert(!Q8 || D == 128, "E4M3 queries and keys are built for D = 128");
+    static_assert(F8 == 0 || D == 128, "E4M3 inputs are built for D = 128");
+    static constexpr bool Q8 = F8 >= 1, V8 = F8 == 2;
     // 64-column (128-byte) swizzle blocks per row; with D = 96 the second block
     // is half used (TMA zero-fills its other half)
     static constexpr int kNDB = (D + 63) / 64;
@@ -110,8 +113,9 @@ template <int D, bool Q8 = false> struct Cfg {
     static constexpr uint32_t kOffKV = kOffQ + 2 * kQKTile;
     static constexpr uint32_t kOffStage = kOffKV + kSlots * kTile;
     static constexpr uint32_t kStageWarp = 32u * 128u;  // 32 rows x 64 bf16 per epilogue warp
-    static constexpr uint32_t kOffBar = kOffStage + 4 * kStageWarp;
-    static constexpr int kNumBars = 25;
+    static constexpr uint32_t kV8Tile = 128u * D;       // an E4M3 V tile (staging)
+    static constexpr uint32_t kOffV8 = kOffStage + 4 * kStageWarp;
+    static constexpr uint32_t kOffBar = kOffV8 + (V8 ? 2 * kV8Tile : 0);
     static constexpr uint32_t kOffL = kOffBar + 8 * 32;       // float [tile][l, m][128]
     static constexpr uint32_t kOffMisc = kOffL + 2 * 2 * 128 * 4; // tmem base, abort flag
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
@@ -125,7 +129,8 @@ template <int D, bool Q8 = false> struct Cfg {
 // mbarrier slots
 enum : int {
     BQ_FULL = 0, BQ_EMPTY = 2, BKV_FULL = 4, BKV_EMPTY = 8, BS_FULL = 12, BP_FULL = 14,
-    BO_FINAL = 16, BO_FREE = 18, BL_FULL = 20, BL_EMPTY = 22, B_DRAIN = 24
+    BO_FINAL = 16, BO_FREE = 18, BL_FULL = 20, BL_EMPTY = 22, B_DRAIN = 24,
+    BV8_FULL = 26, BV8_EMPTY = 28   // E4M3 V staging ring (F8 = 2)
 };
 
 struct Item {
@@ -507,11 +512,12 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU, bool Q8 = false>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU, int F8 = 0>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
-    using C = Cfg<D, Q8>;
-    static_assert(!Q8 || LD == 0, "E4M3 inputs are head-partitioned");
+    using C = Cfg<D, F8>;
+    constexpr bool Q8 = C::Q8, V8 = C::V8;
+    static_assert(F8 == 0 || (LD == 0 && !CAU), "E4M3 inputs: head-partitioned, non-causal");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -554,9 +560,15 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(BAR(BL_EMPTY + t), 4);
         }
         for (int s = 0; s < C::kSlots; ++s) {
-            mbar_init(BAR(BKV_FULL + s), 1);
+            // E4M3 V: the V slots (odd; K and V alternate) fill when both widening warps arrive
+            mbar_init(BAR(BKV_FULL + s), V8 && (s & 1) ? 2 : 1);
             mbar_init(BAR(BKV_EMPTY + s), 1);
         }
+        if (V8)
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(BAR(BV8_FULL + s), 1);
+                mbar_init(BAR(BV8_EMPTY + s), 2);
+            }
         mbar_init(BAR(B_DRAIN), 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -611,6 +623,15 @@ __global__ void __launch_bounds__(512, 1)
                 for (int j = g.j0; ok && j < g.j1; ++j) {
                     for (int kv = 0; kv < 2; ++kv, ++kv_it) {
                         const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u;
+                        if (V8 && kv) {  // E4M3 V goes to staging slot slot / 2; the widening warps fill the ring slot
+                            const uint32_t s8 = slot >> 1;
+                            ok = bwait(BAR(BV8_EMPTY + s8), ph ^ 1u, abort_flag, kSiteLoadKV);
+                            if (!ok) break;
+                            mbar_arrive_expect_tx(BAR(BV8_FULL + s8), C::kV8Tile);
+                            tma_load_4d(base + C::kOffV8 + s8 * C::kV8Tile, tm.v, BAR(BV8_FULL + s8), 0, w.hl,
+                                        j * 128, w.rb);
+                            continue;
+                        }
                         ok = bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
                         if (!ok) break;
                         mbar_arrive_expect_tx(BAR(BKV_FULL + slot), kv ? C::kTile : C::kQKTile);
@@ -636,10 +657,59 @@ __global__ void __launch_bounds__(512, 1)
                 while (globaltimer_ns() - t0 < 200000ull) {
                 }
             }
+        } else if (V8 && warp >= 2) {
+            // ---------------------------------------------- E4M3 V widening (F8 = 2)
+            // Warp 2 widens columns 0-63 (swizzle block 0), warp 3 columns 64-127.
+            // Lane = 8 * (16-byte input chunk within the half row) + row within an
+            // 8-row swizzle atom, so both the loads (E4M3 staging, 128-byte
+            // swizzle) and the stores (f16 MN-major tile, 128-byte swizzle) hit
+            // eight distinct 16-byte bank groups per quarter warp.
+            const uint32_t e = (uint32_t)lane & 7u;                        // row within the atom
+            const uint32_t u = (uint32_t)(warp - 2) * 4u + ((uint32_t)lane >> 3);  // input chunk 0..7
+            const uint32_t db = u >> 2, c0 = (2u * u) & 7u;                 // output block and chunk pair
+            const uint32_t ld_off = e * 128u + ((u ^ e) << 4);
+            const uint32_t st_off0 = db * C::kBlk + e * 128u + ((c0 ^ e) << 4);
+            const uint32_t st_off1 = db * C::kBlk + e * 128u + (((c0 + 1u) ^ e) << 4);
+            uint32_t v_it = 0;
+            bool ok = true;
+            Sched sch;
+            sched_init(sch, p);
+            Seg g;
+            while (ok && sched_next<CAU>(sch, p, g)) {
+                for (int j = g.j0; ok && j < g.j1; ++j, ++v_it) {
+                    const uint32_t kv_it = 2u * v_it + 1u;  // V tiles sit at odd ring positions
+                    const uint32_t slot = kv_it % C::kSlots, ph = (kv_it / C::kSlots) & 1u, s8 = slot >> 1;
+                    ok = warp_bwait(BAR(BV8_FULL + s8), ph, abort_flag, kSiteLoadKV) &&
+                         warp_bwait(BAR(BKV_EMPTY + slot), ph ^ 1u, abort_flag, kSiteLoadKV);
+                    if (!ok) break;
+                    const uint32_t src = base + C::kOffV8 + s8 * C::kV8Tile + ld_off;
+                    const uint32_t dst = sKV + slot * C::kTile;
+#pragma unroll 2
+                    for (uint32_t rg = 0; rg < 16; ++rg) {  // 8-row groups
+                        uint32_t x0, x1, x2, x3, y0, y1, y2, y3, y4, y5, y6, y7;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                     : "r"(src + rg * 1024u)
+                                     : "memory");
+                        e4m3x4_to_f16x4(x0, y0, y1);
+                        e4m3x4_to_f16x4(x1, y2, y3);
+                        e4m3x4_to_f16x4(x2, y4, y5);
+                        e4m3x4_to_f16x4(x3, y6, y7);
+                        st_shared_v4(dst + rg * 1024u + st_off0, y0, y1, y2, y3);
+                        st_shared_v4(dst + rg * 1024u + st_off1, y4, y5, y6, y7);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(BAR(BV8_EMPTY + s8));
+                        mbar_arrive(BAR(BKV_FULL + slot));
+                    }
+                }
+            }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idS = Q8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, 0);
-            constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
+            constexpr uint32_t idO = V8 ? idesc_f16_f32(128, D, 1) : idesc_bf16_f32(128, D, 1);
             // Descriptors differ only in the start-address field (address >> 4 in
             // the low 14 bits), so each MMA adds a compile-time offset to a base.
             const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
@@ -851,8 +921,8 @@ __global__ void __launch_bounds__(512, 1)
                         e3 = ex2_approx(e3);
                         acc0 = fadd2(acc0, f2pack(e0, e1));
                         acc1 = fadd2(acc1, f2pack(e2, e3));
-                        pk[i] = pack_bf16x2(e0, e1);
-                        pk[i + 1] = pack_bf16x2(e2, e3);
+                        pk[i] = V8 ? pack_f16x2(e0, e1) : pack_bf16x2(e0, e1);
+                        pk[i + 1] = V8 ? pack_f16x2(e2, e3) : pack_bf16x2(e2, e3);
                     }
                     tmem_st32(tS + 32 * hf, pk);
                 }
@@ -1018,11 +1088,11 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false, bool Q8 = false>
+template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false, int F8 = 0>
 static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU, Q8>;
-    using CQ = Cfg<D, Q8>;
+    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU, F8>;
+    using CQ = Cfg<D, F8>;
     // The shared-memory limit is raised once per device and instance: setting a
     // function attribute before every launch makes each launch start much later.
     static std::atomic<uint64_t> configured{0};

@@ -102,9 +102,11 @@ XS_DECLARE_ATTN_ENTRY(128)
 XS_DECLARE_ATTN_ENTRY(256)
 cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                          cudaStream_t stream);
-// E4M3 queries and keys (maps q, k over bytes), bf16 values; D = 128 only.
-cudaError_t launch_attention_q8_d128(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+// E4M3 inputs, D = 128 only (xs_attn_f8.cu): f8 = 1 for E4M3 q and k (maps over
+// bytes) with bf16 v, f8 = 2 for E4M3 q, k and v.
+cudaError_t launch_attention_f8_d128(int f8, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                      cudaStream_t stream);
+cudaError_t read_error_word_f8(unsigned int *value, bool clear);
 
 // Sets the calling thread's xs_last_error() text; returns `status`.
 int report_error(int status, const char *message);

@@ -162,6 +162,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
            | ((uint32_t)(M >> 4) << 24);          // M / 16
 }
 
+// Same with f16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major) {
+    return (1u << 4)                              // D format: F32
+           | ((uint32_t)b_mn_major << 16)         // B major-ness
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
 // both K-major, fp32 accumulator, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
@@ -280,6 +288,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Round two fp32 to f16 (nearest even) and pack: `lo` in bits 0-15, `hi` in 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four E4M3 bytes (byte i = element i) -> four f16, exactly (every E4M3 value,
+// subnormals included, is an f16 value): elements 0, 1 in `lo`, 2, 3 in `hi`.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t in, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(in));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x0), "r"(x1), "r"(x2), "r"(x3) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (tensor-core operand reads) that synchronise with it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ registers

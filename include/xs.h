@@ -227,6 +227,22 @@ xs_status xs_attn_q8(const void *q8, const void *k8, const void *v, void *out, i
                      float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The same with E4M3 values as well (an extension; the X-Stage paper evaluates
+ * bf16 only): q8, k8 and v8 are head-partitioned [P][B][S][Hl][D] E4M3 bytes,
+ * out bf16 as for xs_attn_a2a_q8 / xs_attn_q8. Each V tile is widened exactly
+ * to f16 on chip, P is rounded to f16 (10 mantissa bits, against bf16's 7 in
+ * the other calls) and P V runs as f16 x f16 with fp32 accumulation. A
+ * dequantisation factor of v8 multiplies the output; apply it to out (or fold
+ * it into the next operation). D = 128 only. xs_attn_a2a_qkv8 is bit-identical
+ * to xs_a2a_permute(xs_attn_qkv8(...)). XS_ERR_ALIAS when out overlaps the
+ * B*S*H*D bytes of q8, k8 or v8.
+ */
+xs_status xs_attn_a2a_qkv8(const void *q8, const void *k8, const void *v8, void *out, int B, int S, int H, int D,
+                           int P, float scale, void *workspace, size_t workspace_bytes, void *stream);
+xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out, int B, int S, int H, int D, int P,
+                       float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The fused call (xs_attn_a2a, whole-item schedule) with its epilogue traced:
  * the per-tile record the paper's section 5.2.3 uses to measure each output
  * tile's sender-visible store span, and the section 4.3 audit its Q-loop gap.

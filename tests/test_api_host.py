@@ -167,6 +167,11 @@ def test_q8_argument_checks(xs):
         assert f(fn=fn, scale=0.0) == xs.XS_ERR_SHAPE
         assert f(fn=fn, ws=None, nb=64) == xs.XS_ERR_WORKSPACE
         assert f(fn=fn, B=0) == xs.XS_OK
+    g = lambda o=O, **kw: xs.attn_a2a_qkv8(Q, K, V, o, 1, 256, 8, kw.get("D", 128), 4, 0.088, None, 0,
+                                           check=False)
+    assert g(D=64) == xs.XS_ERR_UNSUPPORTED
+    assert g(o=V + 262144 - 16) == xs.XS_ERR_ALIAS     # v8 holds one byte per element too
+    assert xs.attn_qkv8(Q, K, 0, O, 1, 256, 8, 128, 4, 0.088, check=False) == xs.XS_ERR_NULL
     # q8 and k8 hold one byte per element: B*S*H*D = 262144 bytes here
     assert f(o=Q + 262144 - 16) == xs.XS_ERR_ALIAS
     assert f(o=K + 262144 - 16) == xs.XS_ERR_ALIAS
@@ -176,3 +181,4 @@ def test_q8_argument_checks(xs):
     if not torch.cuda.is_available():
         # past the end of q8: only the missing GPU stops the call
         assert f(o=Q + 262144) in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
+        assert g(o=V + 262144) in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
