@@ -91,7 +91,7 @@ def workload_bytes(w) -> int:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("xs_attn_kernel.cuh", "xs_attn_d128.cu", "xs_ptx.cuh"):
+    for name in ("xs_attn_kernel.cuh", "xs_attn_d128.cu", "xs_attn_f8.cu", "xs_ptx.cuh"):
         with open(os.path.join(ROOT, "comm_comp_fusion_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
