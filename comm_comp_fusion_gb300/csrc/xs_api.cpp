@@ -237,7 +237,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     xs::AttnParams p;
     p.ld_rows = gcd_int(S / P, 128);
     xs::OperandMaps<1> head_maps;
-    xs::OperandMaps<xs::kMaxRanks> rank_maps;
+    xs::OperandMaps<xs::kSeqMaps> rank_maps;
     if (layout == 0) {
         if ((st = make_head_map(&head_maps.q[0], q, B, S, H, D, P, "q", o.f8 ? 1 : 2)) ||
             (st = make_head_map(&head_maps.k[0], k, B, S, H, D, P, "k", o.f8 ? 1 : 2)) ||
@@ -245,11 +245,16 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
             return st;
     } else {
         memset(&rank_maps, 0, sizeof rank_maps);
+        // entries r: boxes of ld_rows rows; entries kMaxRanks + r: 128-row boxes
+        // for tiles inside one rank's slice (none when Sl < 128)
         for (int r = 0; r < P; ++r)
-            if ((st = make_rank_map(&rank_maps.q[r], q, r, B, S, H, D, P, p.ld_rows, "q")) ||
-                (st = make_rank_map(&rank_maps.k[r], k, r, B, S, H, D, P, p.ld_rows, "k")) ||
-                (st = make_rank_map(&rank_maps.v[r], v, r, B, S, H, D, P, p.ld_rows, "v")))
-                return st;
+            for (int big = 0; big < (S / P >= 128 ? 2 : 1); ++big) {
+                const int e = big * xs::kMaxRanks + r, rows = big ? 128 : p.ld_rows;
+                if ((st = make_rank_map(&rank_maps.q[e], q, r, B, S, H, D, P, rows, "q")) ||
+                    (st = make_rank_map(&rank_maps.k[e], k, r, B, S, H, D, P, rows, "k")) ||
+                    (st = make_rank_map(&rank_maps.v[e], v, r, B, S, H, D, P, rows, "v")))
+                    return st;
+            }
     }
     p.B = B;
     p.S = S;

@@ -70,7 +70,7 @@ cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const Attn
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
+cudaError_t launch_ulysses(int D, const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,
                            cudaStream_t stream) {
     if (D == 256) return launch_ulysses_d256(maps, p, grid, stream);
     if (D == 128) return launch_ulysses_d128(maps, p, grid, stream);

@@ -475,13 +475,20 @@ __device__ __forceinline__ void load_rows_head(uint32_t dst, const CUtensorMap *
 // Sequence-partitioned tensor: the rows are read where the sequence partition
 // keeps them, in the slice of the rank that owns each token (the pre-attention
 // All-to-All of Ulysses, section 4.3, Figure 5 (a-c)), through that rank's
-// tensor map. Token s0 is row `sl` of rank `rs`'s slice; the box height
-// p.ld_rows divides Sl, so no box straddles two ranks. Rows at or past S (the
-// absent second tile of an odd tile count) lie outside every map and are
-// zero-filled.
+// tensor maps. Token s0 is row `sl` of rank `rs`'s slice. A tile inside one
+// rank's slice takes one 128-row box per swizzle block; a tile that straddles
+// ranks takes boxes of p.ld_rows rows, which divides Sl, so no box straddles
+// two ranks. Rows at or past S (the absent second tile of an odd tile count,
+// the tail of a partial last tile) lie outside every map and are zero-filled.
 template <int D>
 __device__ __forceinline__ void load_rows_seq(uint32_t dst, const CUtensorMap *maps, uint32_t bar,
                                               const AttnParams &p, int b, int h, int rs, int sl) {
+    if (sl + 128 <= p.Sl) {
+#pragma unroll
+        for (int db = 0; db < Cfg<D>::kNDB; ++db)
+            tma_load_4d(dst + db * Cfg<D>::kBlk, maps + kMaxRanks + rs, bar, db * 64, h, sl, b);
+        return;
+    }
     for (int y = 0; y < 128; y += p.ld_rows) {
 #pragma unroll
         for (int db = 0; db < Cfg<D>::kNDB; ++db)
@@ -502,7 +509,7 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
 
 template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU>
 __global__ void __launch_bounds__(512, 1)
-    attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kMaxRanks : 1> tm, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kSeqMaps : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -546,6 +553,11 @@ __global__ void __launch_bounds__(512, 1)
             prefetch_tmap(&tm.q[r]);
             prefetch_tmap(&tm.k[r]);
             prefetch_tmap(&tm.v[r]);
+            if (LD && p.Sl >= 128) {
+                prefetch_tmap(&tm.q[kMaxRanks + r]);
+                prefetch_tmap(&tm.k[kMaxRanks + r]);
+                prefetch_tmap(&tm.v[kMaxRanks + r]);
+            }
         }
     }
     if (warp == 2) {
@@ -963,7 +975,7 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false>
-static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
+static cudaError_t launch_one(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
     auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU>;
     // The shared-memory limit is raised once per device and instance: setting a
@@ -996,7 +1008,7 @@ static cudaError_t launch_one(const OperandMaps<LD ? kMaxRanks : 1> &maps, const
 // The ragged instances (S not a multiple of 128) carry the key mask and the
 // row guard; the others compile without them.
 template <int D, int EPI, int LD>
-static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const AttnParams &p, int grid,
+static cudaError_t launch_t(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                             cudaStream_t stream) {
     return p.kv_tail < 128 ? launch_one<D, EPI, LD, 0, true>(maps, p, grid, stream)
                            : launch_one<D, EPI, LD, 0, false>(maps, p, grid, stream);
@@ -1009,7 +1021,7 @@ static cudaError_t launch_t(const OperandMaps<LD ? kMaxRanks : 1> &maps, const A
                                       cudaStream_t stream) {                                                      \
         return epi ? launch_t<D, 1, 0>(maps, p, grid, stream) : launch_t<D, 0, 0>(maps, p, grid, stream);          \
     }                                                                                                             \
-    cudaError_t launch_ulysses_d##D(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,             \
+    cudaError_t launch_ulysses_d##D(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream) {                                                        \
         return launch_t<D, 1, 1>(maps, p, grid, stream);                                                          \
     }                                                                                                             \

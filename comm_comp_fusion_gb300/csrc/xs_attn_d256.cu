@@ -13,7 +13,7 @@ cudaError_t launch_attention_d256(int epi, const OperandMaps<1> &maps, const Att
                                   cudaStream_t stream) {
     return one::launch_attention_d256(epi, maps, p, grid, stream);
 }
-cudaError_t launch_ulysses_d256(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
+cudaError_t launch_ulysses_d256(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,
                                 cudaStream_t stream) {
     return one::launch_ulysses_d256(maps, p, grid, stream);
 }

@@ -63,12 +63,15 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced);
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms);
 
 // Most simulated ranks a call with sequence-partitioned inputs accepts: the
-// kernel takes one TMA tensor map per source rank and operand as a parameter.
+// kernel takes two TMA tensor maps per source rank and operand as a parameter.
 constexpr int kMaxRanks = 8;
+constexpr int kSeqMaps = 2 * kMaxRanks;
 
 // TMA tensor maps of Q, K and V. NM = 1: one map per operand over the
-// head-partitioned tensor. NM = kMaxRanks: one map per source rank over that
-// rank's sequence-partitioned slice (entries past P unused).
+// head-partitioned tensor. NM = kSeqMaps: maps over each source rank's
+// sequence-partitioned slice; entry r (r < P) has boxes of ld_rows = gcd(Sl, 128)
+// rows, which never straddle two ranks, and entry kMaxRanks + r boxes of 128 rows
+// for tiles that lie inside rank r's slice (used only when Sl >= 128).
 template <int NM> struct OperandMaps {
     CUtensorMap q[NM], k[NM], v[NM];
 };
@@ -84,14 +87,14 @@ cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const Attn
                           cudaStream_t stream);
 // Sequence-partitioned inputs (the pre-attention All-to-All done by the loads),
 // sequence-partitioned output.
-cudaError_t launch_ulysses(int D, const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,
+cudaError_t launch_ulysses(int D, const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,
                            cudaStream_t stream);
 
 // Per-head-dimension instances (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu).
 #define XS_DECLARE_ATTN_ENTRY(D)                                                                                  \
     cudaError_t launch_attention_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
                                       cudaStream_t stream);                                                       \
-    cudaError_t launch_ulysses_d##D(const OperandMaps<kMaxRanks> &maps, const AttnParams &p, int grid,             \
+    cudaError_t launch_ulysses_d##D(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream);                                                         \
     cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
                                    cudaStream_t stream);                                                          \

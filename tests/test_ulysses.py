@@ -85,6 +85,11 @@ ULYSSES = [
     (1, 1024, 16, 128, 8, 1.0, 128 ** -0.5),   # Sl = 128: one tile per rank
     (1, 512, 2, 128, 2, 2.0, 0.35),            # very peaked softmax
     (1, 4096, 4, 128, 2, 1.0, 128 ** -0.5),    # few items: the balanced schedule splits every item
+    # 128-row boxes for tiles inside one rank's slice, small boxes where a tile straddles ranks
+    (1, 4032, 8, 128, 8, 1.0, 128 ** -0.5),    # the ragged DiT shape: Sl = 504, boxes of 8 rows, partial last tile
+    (1, 1200, 6, 128, 3, 1.0, 128 ** -0.5),    # Sl = 400: boxes of 16 rows, ragged S
+    (1, 2000, 4, 256, 2, 1.0, 256 ** -0.5),    # D = 256 (single-tile kernel), Sl = 1000: boxes of 8 rows
+    (1, 1536, 4, 96, 4, 1.0, 96 ** -0.5),      # D = 96, Sl = 384: only 128-row boxes
 ]
 
 
