@@ -15,7 +15,9 @@
 //   * section 4.3, Figure 5 (a-c): optionally (LD = 1) the pre-attention
 //     All-to-All is folded into the loads too: Q, K and V rows of head h are
 //     fetched from the sequence-partitioned slices of the ranks that own them,
-//     through one TMA tensor map per rank.
+//     through TMA tensor maps per rank;
+//   * causal (CAU) and ragged (RAG, S not a multiple of 128) instances, and
+//     E4M3 inputs (F8, D = 128): queries and keys, or queries, keys and values.
 //
 // Softmax is computed online (running row max m, running sum l, rescaling of
 // O when m grows), in base 2 with scale*log2(e) folded into one FMA. The row
@@ -27,12 +29,13 @@
 //   warp 0      TMA producer: Q tile pair, then K_j, V_j into a 4-slot ring
 //   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
 //   warp 2      tensor-memory allocator
+//   warps 2-3   (F8 = 2) widen each E4M3 V tile to f16 in its ring slot
 //   warps 4-7   softmax of query tile 0 (one thread per row)
 //   warps 8-11  softmax of query tile 1
 //   warps 12-15 epilogue: O/l -> bf16 -> shared-memory transpose -> coalesced
 //               16-byte stores into the destination rows
-// Tensor memory (512 columns): S0 | S1 | O0 | O1; P_t (bf16) overwrites the
-// first half of S_t after the softmax has read it.
+// Tensor memory (512 columns): S0 | S1 | O0 | O1; P_t (bf16, or f16 with F8 = 2)
+// overwrites the first half of S_t after the softmax has read it.
 //
 // Schedule: whole items round-robin, then (when the caller passes a workspace)
 // the last one to two waves of (item, K/V tile) units split evenly over all
