@@ -40,7 +40,7 @@ EXPORTS = ("xs_attn_a2a", "xs_attn", "xs_a2a_permute", "xs_a2a_permute_inverse",
            "xs_attn_a2a_ws", "xs_attn_ws", "xs_attn_workspace_size", "xs_attn_a2a_noalloc", "xs_last_error",
            "xs_device_status", "xs_selftest_wait_timeout", "xs_version", "xs_attn_a2a_trace", "xs_attn_trace_layout",
            "xs_attn_causal_a2a", "xs_attn_causal", "xs_attn_a2a_q8", "xs_attn_q8",
-           "xs_attn_a2a_qkv8", "xs_attn_qkv8",
+           "xs_attn_a2a_qkv8", "xs_attn_qkv8", "xs_attn_a2a_host", "xs_attn_host",
            # include/xs_burst.h
            "xs_burst_rec_bytes", "xs_burst_gap")
 
@@ -94,6 +94,10 @@ def _load() -> ctypes.CDLL:
     lib.xs_attn_a2a_q8.restype = i
     lib.xs_attn_q8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_q8.restype = i
+    lib.xs_attn_a2a_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_a2a_host.restype = i
+    lib.xs_attn_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.xs_attn_host.restype = i
     lib.xs_attn_a2a_qkv8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.xs_attn_a2a_qkv8.restype = i
     lib.xs_attn_qkv8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
@@ -126,6 +130,17 @@ def _ptr(x):
     if isinstance(x, int):
         return x
     return x.data_ptr()
+
+
+def _hptr(x):
+    """Address of a host buffer: a CPU torch tensor, a C-contiguous numpy array or an int."""
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if not x.flags["C_CONTIGUOUS"]:
+        raise ValueError("host buffers must be C-contiguous")
+    return x.ctypes.data
 
 
 def _stream(stream, *tensors):
@@ -207,6 +222,28 @@ def attn_qkv8(q8, k8, v8, out, B, S, H, D, P, scale, workspace=None, workspace_b
     """Attention only with E4M3 queries, keys and values (``xs_attn_qkv8``), head-partitioned output."""
     st = lib.xs_attn_qkv8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
                           _nbytes(workspace, workspace_bytes), _stream(stream, v8, out))
+    return _check(st) if check else st
+
+
+def attn_a2a_host(q_host, k_host, v_host, out_host, q, k, v, out, B, S, H, D, P, scale, workspace=None,
+                  workspace_bytes=None, stream=None, check=True):
+    """Fused call on host-memory inputs and output (``xs_attn_a2a_host``): copies in,
+    compute and copies out pipelined over rank chunks; q, k, v, out are device
+    staging buffers. Host buffers are torch CPU tensors (pinned for overlap),
+    numpy arrays or raw addresses."""
+    st = lib.xs_attn_a2a_host(_hptr(q_host), _hptr(k_host), _hptr(v_host), _hptr(out_host), _ptr(q), _ptr(k),
+                              _ptr(v), _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace),
+                              _nbytes(workspace, workspace_bytes), _stream(stream, q, out))
+    return _check(st) if check else st
+
+
+def attn_host(q_host, k_host, v_host, out_host, q, k, v, out, B, S, H, D, P, scale, workspace=None,
+              workspace_bytes=None, stream=None, check=True):
+    """Attention only on host-memory inputs and output (``xs_attn_host``), pipelined like
+    ``attn_a2a_host``."""
+    st = lib.xs_attn_host(_hptr(q_host), _hptr(k_host), _hptr(v_host), _hptr(out_host), _ptr(q), _ptr(k), _ptr(v),
+                          _ptr(out), B, S, H, D, P, float(scale), _ptr(workspace), _nbytes(workspace, workspace_bytes),
+                          _stream(stream, q, out))
     return _check(st) if check else st
 
 

@@ -188,7 +188,108 @@ struct CallOpts {
     size_t trace_bytes = 0;
     bool causal = false;
     int f8 = 0;               // 1: q and k hold E4M3 bytes; 2: q, k and v do (D = 128, layout 0)
+    // host buffers: copy in, compute and copy out pipelined over rank chunks
+    // (q, k, v, out are then the device staging buffers)
+    const void *hq = nullptr, *hk = nullptr, *hv = nullptr;
+    void *hout = nullptr;
 };
+
+// Internal streams and events of the host-buffer pipeline, one set per device,
+// created on first use. The mutex keeps one call's enqueue sequence whole.
+constexpr int kMaxChunks = 16;
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, in[kMaxChunks] = {}, comp[kMaxChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+xs_status pipe_init(HostPipe &hp) {
+    if (hp.ready) return XS_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+    for (int c = 0; c < kMaxChunks && e == cudaSuccess; ++c) {
+        e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.comp[c], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return fail_cuda("creating the host pipeline's streams and events", e);
+    hp.ready = true;
+    return XS_OK;
+}
+
+cudaError_t launch_any(const CallOpts &o, int D, const xs::OperandMaps<1> &maps, const xs::AttnParams &p, int grid,
+                       cudaStream_t s) {
+    if (o.causal) return xs::launch_causal(D, o.epi, maps, p, grid, s);
+    if (o.f8) return xs::launch_attention_f8_d128(o.f8, o.epi, maps, p, grid, s);
+    return xs::launch_attention(D, o.epi, maps, p, grid, s);
+}
+
+// The host-buffer call: ranks are split into up to kMaxChunks chunks. Chunk c's
+// q, k, v slices (contiguous in the head-partitioned layout) are copied in on
+// the pipeline's h2d stream; the caller's stream waits for them and runs the
+// attention kernel over that chunk's work items only; the d2h stream then
+// copies the chunk's output out: the columns of its heads in every row of the
+// sequence-partitioned output (one 2-D copy), or its contiguous slice of the
+// head-partitioned one. Copies of later chunks overlap the compute of earlier
+// ones. The caller's stream finally waits for the last copy out.
+xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const void *v, void *out, size_t qk_bytes,
+                        size_t v_bytes, size_t bytes, int D, xs::AttnParams p, const xs::OperandMaps<1> &maps,
+                        const DeviceInfo &info, int dev, cudaStream_t s) {
+    HostPipe &hp = g_pipe[dev];
+    std::lock_guard<std::mutex> lk(hp.mu);
+    xs_status st = pipe_init(hp);
+    if (st) return st;
+    const int P = p.P, per_rank = p.n_items / P;
+    const int chunks = P < kMaxChunks ? P : kMaxChunks;
+    const size_t q_rank = qk_bytes / P, v_rank = v_bytes / P, o_rank = bytes / P;
+    const size_t head_row = (size_t)D * 2, pitch = (size_t)p.H * head_row;
+    const char *hq = static_cast<const char *>(o.hq), *hk = static_cast<const char *>(o.hk);
+    const char *hv = static_cast<const char *>(o.hv);
+    char *hout = static_cast<char *>(o.hout);
+    const char *dq = static_cast<const char *>(q), *dk = static_cast<const char *>(k);
+    const char *dv = static_cast<const char *>(v);
+    char *dout = static_cast<char *>(out);
+    cudaError_t e = cudaEventRecord(hp.start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.start, 0);
+    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+        const int r0 = (int)((long long)c * P / chunks), r1 = (int)((long long)(c + 1) * P / chunks);
+        const int nr = r1 - r0;
+        e = cudaMemcpyAsync((void *)(dq + r0 * q_rank), hq + r0 * q_rank, nr * q_rank, cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync((void *)(dk + r0 * q_rank), hk + r0 * q_rank, nr * q_rank, cudaMemcpyHostToDevice,
+                                hp.h2d);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync((void *)(dv + r0 * v_rank), hv + r0 * v_rank, nr * v_rank, cudaMemcpyHostToDevice,
+                                hp.h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.in[c], hp.h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in[c], 0);
+        if (e != cudaSuccess) break;
+        xs::AttnParams pc = p;
+        pc.item0 = r0 * per_rank;
+        pc.n_items = nr * per_rank;
+        if (pc.ws_rec) pc.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
+        const int grid = xs::attn_schedule(pc, info.num_sms, pc.ws_rec != nullptr && !o.causal);
+        e = launch_any(o, D, maps, pc, grid, s);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.comp[c], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.comp[c], 0);
+        if (e != cudaSuccess) break;
+        if (o.epi) {
+            const size_t col = (size_t)r0 * p.Hl * head_row;
+            e = cudaMemcpy2DAsync(hout + col, pitch, dout + col, pitch, (size_t)nr * p.Hl * head_row,
+                                  (size_t)P * p.B * p.Sl, cudaMemcpyDeviceToHost, hp.d2h);
+        } else {
+            e = cudaMemcpyAsync(hout + r0 * o_rank, dout + r0 * o_rank, nr * o_rank, cudaMemcpyDeviceToHost, hp.d2h);
+        }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hp.done, hp.d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.done, 0);
+    if (e != cudaSuccess) return fail_cuda("host-buffer pipeline", e);
+    return XS_OK;
+}
 
 // layout 0: q, k, v head-partitioned, out as `epi` says. layout 1: q, k, v and
 // out sequence-partitioned (both All-to-Alls fused; `epi` must be 1).
@@ -199,6 +300,9 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     const size_t ws_bytes = o.ws_bytes, trace_bytes = o.trace_bytes;
     const bool causal = o.causal;
     if (!q || !k || !v || !out) return fail(XS_ERR_NULL, "q, k, v and out must be non-NULL");
+    const bool host = o.hq || o.hk || o.hv || o.hout;
+    if (host && (!o.hq || !o.hk || !o.hv || !o.hout))
+        return fail(XS_ERR_NULL, "host q, k, v and out must all be non-NULL");
     size_t bytes = 0;
     xs_status st = check_shape(B, S, H, D, P, true, &bytes);
     if (st) return st;
@@ -224,6 +328,19 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         if (overlaps(ws, ws_bytes, q, qk_bytes) || overlaps(ws, ws_bytes, k, qk_bytes) || overlaps(ws, ws_bytes, v, v_bytes) ||
             overlaps(ws, ws_bytes, out, bytes))
             return fail(XS_ERR_WORKSPACE, "workspace overlaps q, k, v or out");
+    }
+    if (host) {
+        if (layout || trace) return fail(XS_ERR_UNSUPPORTED, "host buffers take head-partitioned inputs, untraced");
+        const void *hs[4] = {o.hq, o.hk, o.hv, o.hout};
+        const size_t hb[4] = {qk_bytes, qk_bytes, v_bytes, bytes};
+        const void *ds[4] = {q, k, v, out};
+        for (int i = 0; i < 4; ++i)
+            for (int j = 0; j < 4; ++j)
+                if (overlaps(hs[i], hb[i], ds[j], hb[j]))
+                    return fail(XS_ERR_ALIAS, "a host buffer overlaps a device buffer");
+        if (overlaps(o.hout, bytes, o.hq, qk_bytes) || overlaps(o.hout, bytes, o.hk, qk_bytes) ||
+            overlaps(o.hout, bytes, o.hv, v_bytes))
+            return fail(XS_ERR_ALIAS, "host out overlaps host q, k or v");
     }
     if (bytes == 0) return XS_OK;
 
@@ -285,10 +402,11 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         p.ws_cnt = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + rec);
         p.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
     }
-    const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr && !causal);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (host) return host_pipeline(o, q, k, v, out, qk_bytes, v_bytes, bytes, D, p, head_maps, info, dev, s);
+    const int grid = xs::attn_schedule(p, info.num_sms, ws != nullptr && !causal);
     if (causal) {
-        cudaError_t e = xs::launch_causal(D, epi, head_maps, p, grid, s);
+        cudaError_t e = launch_any(o, D, head_maps, p, grid, s);
         if (e != cudaSuccess) return fail_cuda("causal attention launch", e);
         return XS_OK;
     }
@@ -303,9 +421,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         if (e != cudaSuccess) return fail_cuda("traced attention launch", e);
         return XS_OK;
     }
-    cudaError_t e = o.f8          ? xs::launch_attention_f8_d128(o.f8, epi, head_maps, p, grid, s)
-                    : layout == 0 ? xs::launch_attention(D, epi, head_maps, p, grid, s)
-                                  : xs::launch_ulysses(D, rank_maps, p, grid, s);
+    cudaError_t e = layout == 0 ? launch_any(o, D, head_maps, p, grid, s) : xs::launch_ulysses(D, rank_maps, p, grid, s);
     if (e != cudaSuccess) return fail_cuda("attention launch", e);
     return XS_OK;
 }
@@ -410,6 +526,33 @@ xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out
     o.ws_bytes = workspace_bytes;
     o.f8 = 2;
     return attention_call(q8, k8, v8, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_a2a_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, void *q,
+                           void *k, void *v, void *out, int B, int S, int H, int D, int P, float scale,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.epi = 1;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.hq = q_host;
+    o.hk = k_host;
+    o.hv = v_host;
+    o.hout = out_host;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
+}
+
+xs_status xs_attn_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, void *q, void *k,
+                       void *v, void *out, int B, int S, int H, int D, int P, float scale, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    CallOpts o;
+    o.ws = workspace;
+    o.ws_bytes = workspace_bytes;
+    o.hq = q_host;
+    o.hk = k_host;
+    o.hv = v_host;
+    o.hout = out_host;
+    return attention_call(q, k, v, out, B, S, H, D, P, scale, stream, o);
 }
 
 xs_status xs_attn_a2a_trace(const void *q, const void *k, const void *v, void *out, int B, int S, int H, int D,

@@ -126,6 +126,7 @@ struct Item {
 };
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     Item it;
+    item += p.item0;  // scheduler items are local to the call's rank range
     it.qt = item % p.n_qt;
     const int head = item / p.n_qt;
     it.hl = head % p.Hl;

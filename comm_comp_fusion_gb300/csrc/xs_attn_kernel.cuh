@@ -141,6 +141,7 @@ struct Item {
 };
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     Item it;
+    item += p.item0;  // scheduler items are local to the call's rank range
     it.pair = item % p.n_pairs;
     const int head = item / p.n_pairs;
     it.hl = head % p.Hl;

@@ -26,7 +26,8 @@ struct AttnParams {
     int n_pairs;  // work items per head           (ceil(n_qt / 2))
     int n_kv;     // 128-row K/V tiles per head    (ceil(S / 128))
     int kv_tail;  // keys in the last K/V tile (128 unless S is ragged); later columns are masked
-    int n_items;  // P * B * Hl * n_pairs (P * B * Hl * n_qt for single-tile items)
+    int n_items;  // P * B * Hl * n_pairs (P * B * Hl * n_qt for single-tile items), or a rank range's share
+    int item0 = 0;  // global index of work item 0 (a call over the ranks from rank0 on: rank0 * B * Hl * items per head)
     float scale_log2;  // scale * log2(e): softmax runs in base 2
     uint16_t *out;
     int n_dp;              // round-robin waves of whole items

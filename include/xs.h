@@ -243,6 +243,43 @@ xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out
                        float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The fused call (xs_attn_a2a_host) and attention only (xs_attn_host) on inputs
+ * and output in HOST memory, for callers whose tensors live on the host. The X-Stage
+ * paper has no counterpart; these calls exist for deployment. The copies are pipelined
+ * with the compute: the ranks are split into up to 16 chunks. Chunk c's
+ * q, k, v slices are copied in on an internal stream, the caller's stream runs
+ * the attention kernel over that chunk's work items, and an internal stream copies
+ * the chunk's output out while later chunks are copied in and computed. For
+ * xs_attn_a2a_host that output is the columns of the chunk's heads in every row
+ * of the sequence-partitioned output; for xs_attn_host, its slice of the
+ * head-partitioned one.
+ *   q_host, k_host, v_host : head-partitioned [P][B][S][Hl][D] bf16 in host
+ *       memory, read only. out_host : host memory for the output (layouts as for
+ *       xs_attn_a2a / xs_attn), fully overwritten. Page-locked (pinned) host
+ *       memory lets the copies run asynchronously and overlap; pageable memory
+ *       works but the copies then serialise.
+ *   q, k, v, out : device staging buffers of the full sizes, 16-byte aligned,
+ *       overwritten by the call (q, k, v hold the inputs afterwards, out the
+ *       output). No two buffers, host or device, may overlap (XS_ERR_ALIAS).
+ *   workspace, workspace_bytes : as for xs_attn_a2a_ws (NULL, 0: whole-item
+ *       schedule); each chunk's launch uses it in turn. A chunk holds only a
+ *       share of the work items, so without a workspace most SMs idle.
+ * Asynchronous like every call. When the caller's stream reaches the point after
+ * the call, out_host holds the result, and later work on that stream is ordered
+ * after the copies. The first call on a device creates two streams and 34 events
+ * there, kept until the process exits. A per-device lock keeps concurrent calls'
+ * enqueue sequences apart. The result equals that of xs_attn_a2a_ws / xs_attn_ws
+ * with the same workspace up to the rounding of split tiles (the chunks split
+ * differently). Without a workspace it is bit-identical to xs_attn_a2a / xs_attn.
+ */
+xs_status xs_attn_a2a_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, void *q,
+                           void *k, void *v, void *out, int B, int S, int H, int D, int P, float scale,
+                           void *workspace, size_t workspace_bytes, void *stream);
+xs_status xs_attn_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, void *q, void *k,
+                       void *v, void *out, int B, int S, int H, int D, int P, float scale, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * The fused call (xs_attn_a2a, whole-item schedule) with its epilogue traced:
  * the per-tile record the paper's section 5.2.3 uses to measure each output
  * tile's sender-visible store span, and the section 4.3 audit its Q-loop gap.

@@ -182,3 +182,21 @@ def test_q8_argument_checks(xs):
         # past the end of q8: only the missing GPU stops the call
         assert f(o=Q + 262144) in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
         assert g(o=V + 262144) in (xs.XS_ERR_CUDA, xs.XS_ERR_UNSUPPORTED)
+
+
+def test_host_buffer_argument_checks(xs):
+    HQ, HK, HV, HO = 0x60000000, 0x70000000, 0x80000000, 0x90000000
+    f = lambda hq=HQ, ho=HO, q=Q, o=O, **kw: xs.attn_a2a_host(hq, HK, HV, ho, q, K, V, o, kw.get("B", 1),
+                                                              kw.get("S", 256), 8, kw.get("D", 64), 4, 0.125,
+                                                              check=False)
+    assert f(hq=0) == xs.XS_ERR_NULL and "host" in xs.last_error()
+    assert f(ho=0) == xs.XS_ERR_NULL
+    assert f(q=0) == xs.XS_ERR_NULL
+    assert f(hq=Q + 64) == xs.XS_ERR_ALIAS       # host q inside device q
+    assert f(ho=HV + 16) == xs.XS_ERR_ALIAS      # host out overlaps host v
+    assert f(o=O + 8) == xs.XS_ERR_ALIGN
+    assert f(D=80) == xs.XS_ERR_UNSUPPORTED
+    assert f(B=0) == xs.XS_OK
+    g = lambda hv=HV: xs.attn_host(HQ, HK, hv, HO, Q, K, V, O, 1, 256, 8, 64, 4, 0.125, check=False)
+    assert g(hv=0) == xs.XS_ERR_NULL
+    assert g(hv=O) == xs.XS_ERR_ALIAS

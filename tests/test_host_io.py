@@ -1,0 +1,121 @@
+"""The host-buffer calls (xs_attn_a2a_host, xs_attn_host): copies in, compute and
+copies out pipelined over rank chunks. Results must equal the device-buffer
+calls: bit for bit on the whole-item schedule, and within the parity bar (and
+against the oracle) on the balanced one, whose chunks split items differently."""
+import numpy as np
+import pytest
+
+import oracle
+import xsgen
+
+from xs_testlib import SENTINEL, assert_close, from_dev, to_dev
+
+CASES = [
+    (1, 1024, 16, 128, 8),   # one chunk per rank
+    (2, 384, 6, 64, 3),      # B = 2, odd tile count
+    (1, 1024, 32, 64, 32),   # P = 32: 16 chunks of two ranks each
+    (1, 1000, 4, 128, 2),    # ragged S
+    (1, 512, 4, 256, 2),     # D = 256 (single-tile kernel)
+]
+
+
+def _host(a, pinned):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    return t.pin_memory() if pinned else t.clone()
+
+
+def _run(q, k, v, B, S, H, D, P, scale, balanced, pinned, fused=True):
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    n = q.size
+    hq, hk, hv = (_host(a, pinned) for a in (q, k, v))
+    hout = torch.full((n,), -1, dtype=torch.int16)
+    hout = hout.pin_memory() if pinned else hout
+    dq, dk, dv = (torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(3))
+    dout = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    ws, nb = None, 0
+    if balanced:
+        nb = xs.workspace_size(B, S, H, D, P)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    fn = xs.attn_a2a_host if fused else xs.attn_host
+    fn(hq, hk, hv, hout, dq, dk, dv, dout, B, S, H, D, P, scale, ws, nb)
+    torch.cuda.synchronize()
+    assert xs.device_status() == xs.XS_OK, xs.last_error()
+    assert np.array_equal(from_dev(dq), q.ravel()) and np.array_equal(from_dev(dv), v.ravel())
+    got = hout.numpy().view(np.uint16).copy()
+    assert np.array_equal(got, from_dev(dout)), "host out differs from the device staging out"
+    return got, ws, nb
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES)
+def test_host_whole_items_bit_exact(case):
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    B, S, H, D, P = case
+    scale = D ** -0.5
+    q, k, v = xsgen.random_inputs(31 + S + H + P, P, B, S, H, D)
+    ref_f = torch.full((q.size,), -1, dtype=torch.int16, device="cuda")
+    ref_h = torch.full_like(ref_f, -1)
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    xs.attn_a2a(tq, tk, tv, ref_f, B, S, H, D, P, scale)
+    xs.attn(tq, tk, tv, ref_h, B, S, H, D, P, scale)
+    torch.cuda.synchronize()
+    fused, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=False, pinned=True)
+    head, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=False, pinned=True, fused=False)
+    assert not (fused == SENTINEL).any()
+    assert np.array_equal(fused, from_dev(ref_f))
+    assert np.array_equal(head, from_dev(ref_h))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES[:4])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_balanced_parity(case, pinned):
+    B, S, H, D, P = case
+    scale = D ** -0.5
+    q, k, v = xsgen.random_inputs(77 + S + H + P, P, B, S, H, D)
+    ref = oracle.attention(q, k, v, B, S, H, D, P, scale)
+    fused, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=True, pinned=pinned)
+    head, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=True, pinned=pinned, fused=False)
+    assert_close(fused, oracle.a2a(ref, B, S, H, D, P).ravel(), what=f"host fused {case}")
+    assert_close(head, ref.ravel(), what=f"host head {case}")
+
+
+@pytest.mark.gpu
+def test_host_back_to_back_calls_keep_order():
+    """Two calls on one stream with different inputs and the same staging
+    buffers: the second call's copies in must wait for the first call's compute,
+    and each host output must hold its own call's result."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    B, S, H, D, P = 1, 2048, 8, 128, 4
+    scale = D ** -0.5
+    ins = [xsgen.random_inputs(s, P, B, S, H, D) for s in (5, 6)]
+    hin = [[_host(a, True) for a in x] for x in ins]
+    houts = [torch.empty(ins[0][0].size, dtype=torch.int16).pin_memory() for _ in range(2)]
+    dq, dk, dv, dout = (torch.empty(ins[0][0].size, dtype=torch.int16, device="cuda") for _ in range(4))
+    for (hq, hk, hv), ho in zip(hin, houts):
+        xs.attn_a2a_host(hq, hk, hv, ho, dq, dk, dv, dout, B, S, H, D, P, scale)
+    torch.cuda.synchronize()
+    for (q, k, v), ho in zip(ins, houts):
+        ref = torch.empty_like(dout)
+        xs.attn_a2a(to_dev(q), to_dev(k), to_dev(v), ref, B, S, H, D, P, scale)
+        torch.cuda.synchronize()
+        assert np.array_equal(ho.numpy().view(np.uint16), from_dev(ref))
+
+
+@pytest.mark.gpu
+def test_host_dit_full_size_sampled():
+    """The DiT workload through the host path with the balanced schedule, as the
+    bench's end-to-end line runs it; sampled rows against the oracle."""
+    from xs_testlib import sample_rows, seq_rows_of
+    w = xsgen.WORKLOADS[1]
+    B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
+    q, k, v = xsgen.workload_inputs(1)
+    fused, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=True, pinned=True)
+    rows = sample_rows(B, S, H, P, 128, seed=9)
+    ref = oracle.attention_rows(q, k, v, B, S, H, D, P, scale, rows)
+    got = fused.reshape(-1, D)[seq_rows_of(rows, B, S, H, D, P)]
+    assert_close(got.ravel(), ref.ravel(), what="host DiT sampled rows")
