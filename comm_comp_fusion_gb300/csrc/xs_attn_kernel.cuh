@@ -523,6 +523,14 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
+// Ragged S: the keys past S (zero-filled rows of the last K/V tile) take no
+// weight; their scores become -inf in this thread's row of tensor memory.
+// Kept out of line: inlined, it costs the softmax loop 2% at ragged DiT size.
+static __device__ __noinline__ void mask_tail(uint32_t tS, int kv_tail) {
+    for (int c = kv_tail; c < 128; ++c) tmem_st1(tS + (uint32_t)c, f2u(-INFINITY));
+    tmem_st_wait();
+}
+
 template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU, int F8 = 0>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kSeqMaps : 1> tm, const AttnParams p) {
@@ -852,6 +860,7 @@ __global__ void __launch_bounds__(512, 1)
             // causal: this tile's diagonal K/V tile (its last step) is 2p + t
             const int qt_diag = CAU ? 2 * (g.item % p.n_pairs) + t : -1;
             const int nseg = CAU ? min(qt_diag + 1, g.j1 - g.j0) : g.j1 - g.j0;
+            const int jmask = RAG && !CAU ? p.n_kv - 1 - g.j0 : -1;  // the step that holds the last K/V tile
             for (int j = 0; j < nseg; ++j) {
                 ok = warp_bwait(BAR(BS_FULL + t), sph, abort_flag, kSiteSoftS);
                 if (!ok) break;
@@ -861,13 +870,7 @@ __global__ void __launch_bounds__(512, 1)
                 // this thread's row of S: columns 0-63 in sa, 64-127 in sb
                 uint32_t sa[64], sb[64];
 #define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
-                if (RAG && !CAU && g.j0 + j == p.n_kv - 1) {
-                    // keys past S (zero-filled rows of the last K/V tile) take no
-                    // weight: their scores become -inf in tensor memory
-#pragma unroll 1
-                    for (int c = p.kv_tail; c < 128; ++c) tmem_st1(tS + (uint32_t)c, f2u(-INFINITY));
-                    tmem_st_wait();
-                }
+                if (RAG && !CAU && j == jmask) mask_tail(tS, p.kv_tail);
                 tmem_ld64(tS, sa);
                 tmem_ld64(tS + 64, sb);
                 if (CAU && j == qt_diag) {
