@@ -52,7 +52,8 @@ def test_noalloc_matches_workspace_call_on_two_calls():
 def test_noalloc_rejects_shapes_beyond_the_scratch():
     import comm_comp_fusion_gb300 as xs
     fake = [0x10000000, 0x20000000, 0x30000000, 0x40000000]
-    # 16 x 160 heads x 128 pairs of query tiles: the arrival counters alone exceed the scratch
-    st = xs.lib.xs_attn_a2a_noalloc(*fake, 16, 32768, 160, 128, 8, ctypes.c_float(0.1), None)
+    # 80 x 160 heads x 128 pairs of query tiles: the arrival counters alone (32 bytes an
+    # item) exceed the scratch
+    st = xs.lib.xs_attn_a2a_noalloc(*fake, 80, 32768, 160, 128, 8, ctypes.c_float(0.1), None)
     assert st == xs.XS_ERR_WORKSPACE
     assert "built-in scratch" in xs.last_error()
