@@ -79,6 +79,20 @@ xs_status check_device_pointer(const void *ptr, int dev, const char *name) {
     return XS_OK;
 }
 
+// Host-buffer calls: the pointer must not be device memory (pinned or
+// pageable host memory are both fine).
+xs_status check_host_pointer(const void *ptr, const char *name) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(XS_ERR_CUDA, "cudaPointerGetAttributes(%s): %s", name, cudaGetErrorName(e));
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged)
+        return fail(XS_ERR_UNSUPPORTED, "%s must be host memory", name);
+    return XS_OK;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
     return x < y + nb && y < x + na;
@@ -349,6 +363,9 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     if ((st = current_device(&dev, &info))) return st;
     if ((st = check_device_pointer(q, dev, "q")) || (st = check_device_pointer(k, dev, "k")) ||
         (st = check_device_pointer(v, dev, "v")) || (st = check_device_pointer(out, dev, "out")))
+        return st;
+    if (host && ((st = check_host_pointer(o.hq, "q_host")) || (st = check_host_pointer(o.hk, "k_host")) ||
+                 (st = check_host_pointer(o.hv, "v_host")) || (st = check_host_pointer(o.hout, "out_host"))))
         return st;
 
     xs::AttnParams p;

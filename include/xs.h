@@ -257,7 +257,8 @@ xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out
  *       memory, read only. out_host : host memory for the output (layouts as for
  *       xs_attn_a2a / xs_attn), fully overwritten. Page-locked (pinned) host
  *       memory lets the copies run asynchronously and overlap; pageable memory
- *       works but the copies then serialise.
+ *       works but the copies then serialise. Device or managed memory passed
+ *       as a host buffer is rejected with XS_ERR_UNSUPPORTED.
  *   q, k, v, out : device staging buffers of the full sizes, 16-byte aligned,
  *       overwritten by the call (q, k, v hold the inputs afterwards, out the
  *       output). No two buffers, host or device, may overlap (XS_ERR_ALIAS).

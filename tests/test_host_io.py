@@ -119,3 +119,15 @@ def test_host_dit_full_size_sampled():
     ref = oracle.attention_rows(q, k, v, B, S, H, D, P, scale, rows)
     got = fused.reshape(-1, D)[seq_rows_of(rows, B, S, H, D, P)]
     assert_close(got.ravel(), ref.ravel(), what="host DiT sampled rows")
+
+
+@pytest.mark.gpu
+def test_host_call_rejects_device_memory_as_host_buffer():
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    B, S, H, D, P = 1, 256, 4, 64, 2
+    n = B * S * H * D
+    d = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(5)]
+    h = [torch.zeros(n, dtype=torch.int16).pin_memory() for _ in range(4)]
+    st = xs.attn_a2a_host(d[4], h[1], h[2], h[3], d[0], d[1], d[2], d[3], B, S, H, D, P, 0.125, check=False)
+    assert st == xs.XS_ERR_UNSUPPORTED and "q_host" in xs.last_error()
