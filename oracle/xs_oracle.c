@@ -18,8 +18,8 @@
  *    exponentials and sums). The online rescaling recurrence that FlashAttention
  *    uses reaches the same value up to rounding; the oracle does not use it.
  *
- *  - Causal attention (section 4.3 contrasts the DiT setting with "the causal
- *    attention used by typical autoregressive LLMs"; the pages do not write it
+ *  - Causal attention (section 4.3 sets the DiT setting against the causal
+ *    attention of autoregressive language models and does not write the mask
  *    out). Reading taken: query token i of a head sees key tokens j <= i of the
  *    same sequence, so every sum above runs over j = 0..i instead of 0..S-1.
  *
