@@ -37,3 +37,14 @@ def test_bench_line_carries_the_contract(extra):
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["unit"] == "TFLOP/s"
+
+
+@pytest.mark.gpu
+def test_seqlen_sweep_runs_and_reports_every_length():
+    sys.path.insert(0, ROOT)
+    from comm_comp_fusion_gb300 import seqlen_sweep
+    rows = seqlen_sweep.run([1024, 2048], reps=2, H=8, P=4)
+    assert [r["M"] for r in rows] == [1024, 2048]
+    for r in rows:
+        assert r["t_fa_us"] > 0 and r["t_fused_us"] > 0 and r["t_serial_us"] > 0 and r["fused_tflops"] > 0
+    assert "| M | 1024 | 2048 |" in seqlen_sweep.markdown(rows)
