@@ -71,3 +71,18 @@ def test_flop_and_byte_counts():
     w = xsgen.WORKLOADS[1]
     assert bench.workload_flops(w) == 4 * 1 * 24 * 4096 * 4096 * 128
     assert bench.workload_bytes(w) == 1 * 4096 * 24 * 128 * 2
+
+
+@pytest.mark.parametrize("extra", [["--causal"], ["--q8"], ["--qkv8"]], ids=["causal", "q8", "qkv8"])
+def test_reference_arm_modes(extra):
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "0",
+                        "--steps", "1", "--warmup", "3", "--ref-step-seconds", "0.2"] + extra,
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["value"] > 0
+    if "--causal" in extra:
+        assert d["config"]["mask"] == "causal"
+    else:
+        assert "E4M3" in d["config"]["inputs"]
