@@ -11,11 +11,17 @@ import xsgen
 from xs_testlib import SENTINEL, assert_close, from_dev, to_dev
 
 CASES = [
-    (1, 1024, 16, 128, 8),   # one chunk per rank
+    (1, 1024, 16, 128, 8),   # small: one chunk
     (2, 384, 6, 64, 3),      # B = 2, odd tile count
-    (1, 1024, 32, 64, 32),   # P = 32: 16 chunks of two ranks each
+    (1, 1024, 32, 64, 32),   # P = 32 ranks in one chunk
     (1, 1000, 4, 128, 2),    # ragged S
     (1, 512, 4, 256, 2),     # D = 256 (single-tile kernel)
+]
+# large enough for several chunks (about 8 MiB of inputs each, at most one per rank, at most 16)
+MULTI = [
+    (1, 4096, 24, 128, 8),   # the DiT shape: 8 chunks, one rank each
+    (1, 8192, 32, 128, 32),  # 16 chunks of two ranks each
+    (1, 4032, 24, 128, 8),   # ragged S, 8 chunks
 ]
 
 
@@ -49,7 +55,7 @@ def _run(q, k, v, B, S, H, D, P, scale, balanced, pinned, fused=True):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("case", CASES + MULTI)
 def test_host_whole_items_bit_exact(case):
     import torch
     import comm_comp_fusion_gb300 as xs
