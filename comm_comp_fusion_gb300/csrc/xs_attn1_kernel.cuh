@@ -757,59 +757,40 @@ __global__ void __launch_bounds__(512, 1)
                         sbv[i] = 64 + i > row ? ninf : sbv[i];
                     }
                 }
-                float mx0 = fmaxf(u2f(sa[0]), u2f(sa[1])), mx1 = fmaxf(u2f(sa[2]), u2f(sa[3]));
-                float mx2 = fmaxf(u2f(sa[4]), u2f(sa[5])), mx3 = fmaxf(u2f(sa[6]), u2f(sa[7]));
+                // the row max of S (raw scores)
+                auto row_max = [&]() {
+                    float mx0 = fmaxf(u2f(sa[0]), u2f(sa[1])), mx1 = fmaxf(u2f(sa[2]), u2f(sa[3]));
+                    float mx2 = fmaxf(u2f(sa[4]), u2f(sa[5])), mx3 = fmaxf(u2f(sa[6]), u2f(sa[7]));
 #pragma unroll
-                for (int i = 8; i < 64; i += 8) {
-                    mx0 = fmax3(mx0, u2f(sa[i + 0]), u2f(sa[i + 1]));
-                    mx1 = fmax3(mx1, u2f(sa[i + 2]), u2f(sa[i + 3]));
-                    mx2 = fmax3(mx2, u2f(sa[i + 4]), u2f(sa[i + 5]));
-                    mx3 = fmax3(mx3, u2f(sa[i + 6]), u2f(sa[i + 7]));
-                }
-#pragma unroll
-                for (int i = 0; i < 64; i += 8) {
-                    mx0 = fmax3(mx0, u2f(sbv[i + 0]), u2f(sbv[i + 1]));
-                    mx1 = fmax3(mx1, u2f(sbv[i + 2]), u2f(sbv[i + 3]));
-                    mx2 = fmax3(mx2, u2f(sbv[i + 4]), u2f(sbv[i + 5]));
-                    mx3 = fmax3(mx3, u2f(sbv[i + 6]), u2f(sbv[i + 7]));
-                }
-                const float rowmax = fmax3(mx0, mx1, fmaxf(mx2, mx3));
-                const float mnew = rowmax * sl2;
-                float alpha = 1.f;
-                bool need = false;
-                if (j == 0) {
-                    m = mnew;
-                } else if (mnew > m + 8.0f) {
-                    alpha = ex2_approx(m - mnew);
-                    m = mnew;
-                    need = true;
-                }
-                if (__any_sync(0xffffffffu, need)) {
-                    // O must hold the previous step's P V before it is rescaled: the
-                    // step's S was issued ahead of that PV. It is the PV count npv +
-                    // j - 1 (0-based) and at most one phase ahead of this wait.
-                    ok = warp_bwait(BAR(BPV_DONE), (npv + (uint32_t)j - 1u) & 1u, abort_flag, kSiteSoftO);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                        tmem_st32(tO + c, o);
+                    for (int i = 8; i < 64; i += 8) {
+                        mx0 = fmax3(mx0, u2f(sa[i + 0]), u2f(sa[i + 1]));
+                        mx1 = fmax3(mx1, u2f(sa[i + 2]), u2f(sa[i + 3]));
+                        mx2 = fmax3(mx2, u2f(sa[i + 4]), u2f(sa[i + 5]));
+                        mx3 = fmax3(mx3, u2f(sa[i + 6]), u2f(sa[i + 7]));
                     }
-                    l *= alpha;
-                }
+#pragma unroll
+                    for (int i = 0; i < 64; i += 8) {
+                        mx0 = fmax3(mx0, u2f(sbv[i + 0]), u2f(sbv[i + 1]));
+                        mx1 = fmax3(mx1, u2f(sbv[i + 2]), u2f(sbv[i + 3]));
+                        mx2 = fmax3(mx2, u2f(sbv[i + 4]), u2f(sbv[i + 5]));
+                        mx3 = fmax3(mx3, u2f(sbv[i + 6]), u2f(sbv[i + 7]));
+                    }
+                    return fmax3(mx0, mx1, fmaxf(mx2, mx3));
+                };
+                // The running max m is taken at the first step only. Later steps use it
+                // as it stands and check the row sum of p instead: at most 256 means no
+                // p above 2^8, so the max has not passed m + 8 and the rule below would
+                // keep m. Results are the same as with the max taken at every step.
+                if (j == 0) m = row_max() * sl2;
                 // p = exp2(s * scale*log2e - m): paired FMAs, ex2, paired sums, bf16 pairs
-                const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
-                uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+                uint32_t pk[64];
+                float lstep = 0.f;
+                auto exps = [&]() {
+                    const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+                    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const int e = 64 * hf + 2 * i;
+                    for (int i = 0; i < 64; i += 2) {
+                        const int e = 2 * i;
                         float e0, e1, e2, e3;
                         f2unpack(ffma2(f2pack(SV(e), SV(e + 1)), sc2, nm2), e0, e1);
                         f2unpack(ffma2(f2pack(SV(e + 2), SV(e + 3)), sc2, nm2), e2, e3);
@@ -822,14 +803,64 @@ __global__ void __launch_bounds__(512, 1)
                         pk[i] = pack_bf16x2(e0, e1);
                         pk[i + 1] = pack_bf16x2(e2, e3);
                     }
-                    tmem_st32(tS + 32 * hf, pk);
-                }
-#undef SV
-                {
                     float a0, a1;
                     f2unpack(fadd2(acc0, acc1), a0, a1);
-                    l += a0 + a1;
+                    lstep = a0 + a1;
+                };
+                exps();
+                if (j > 0 && __any_sync(0xffffffffu, !(lstep <= 256.0f))) {
+                    // Some row sum passed 256: S is still in TMEM (P has not been
+                    // stored), so reload it, take the max, move m where it grew by
+                    // more than 8 (rescaling O and l) and redo the exponentials.
+                    tmem_ld64(tS, sa);
+                    tmem_ld64(tS + 64, sbv);
+                    if (CAU && j == qt_diag) {
+                        const uint32_t ninf = f2u(-INFINITY);
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            sa[i] = i > row ? ninf : sa[i];
+                            sbv[i] = 64 + i > row ? ninf : sbv[i];
+                        }
+                    }
+                    const float mnew = row_max() * sl2;
+                    float alpha = 1.f;
+                    bool need = false;
+                    if (mnew > m + 8.0f) {
+                        alpha = ex2_approx(m - mnew);
+                        m = mnew;
+                        need = true;
+                    }
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O must hold the previous step's P V before it is rescaled: the
+                        // step's S was issued ahead of that PV. It is the PV count npv +
+                        // j - 1 (0-based) and at most one phase ahead of this wait.
+                        ok = warp_bwait(BAR(BPV_DONE), (npv + (uint32_t)j - 1u) & 1u, abort_flag, kSiteSoftO);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                            tmem_st32(tO + c, o);
+                        }
+                        l *= alpha;
+                    }
+                    exps();
                 }
+                l += lstep;
+                {
+                    uint32_t h0[32], h1[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        h0[i] = pk[i];
+                        h1[i] = pk[32 + i];
+                    }
+                    tmem_st32(tS, h0);
+                    tmem_st32(tS + 32, h1);
+                }
+#undef SV
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();

@@ -24,6 +24,7 @@ CASES = [  # (B, S, H, D, P)
     (1, 2048, 4, 128, 2),
     (2, 1152, 6, 64, 3),
     (1, 2000, 4, 96, 2),
+    (1, 1536, 4, 256, 2),   # the single-query-tile kernel
 ]
 
 
