@@ -908,9 +908,10 @@ __global__ void __launch_bounds__(512, 1)
                 // The running max m is taken at the first step only. Later steps use it
                 // as it stands and check the row sum of p instead: at most 256 means no
                 // p above 2^8, so the max has not passed m + 8 and the rule below would
-                // keep m. Results are the same as with the max taken at every step.
+                // keep m. Results are those of taking the max at every step, but for a
+                // step whose only sizeable p lies within rounding of 256.
                 if (j == 0) m = row_max() * sl2;
-                // p = exp2(s * scale*log2e - m): paired FMAs, ex2, paired sums, bf16 pairs
+                // p = exp2(s * scale*log2e - m): paired FMAs, ex2, paired sums, bf16 (f16) pairs
                 uint32_t pk[64];
                 float lstep = 0.f;
                 auto exps = [&]() {

@@ -86,3 +86,22 @@ def test_reference_arm_modes(extra):
         assert d["config"]["mask"] == "causal"
     else:
         assert "E4M3" in d["config"]["inputs"]
+
+
+def test_kernel_hash_ignores_comments_and_layout():
+    """The recorded ncu traffic is keyed on the kernel's code: comment and layout
+    edits keep the key, a code edit changes it, and string literals are code."""
+    import bench
+    src = 'int f(int a) {\n  // twice\n  return 2 * a; /* x */\n}\nconst char *s = "a//b";\n'
+    same = 'int f(int a) { return 2 * a; }   // doubled\nconst char *s = "a//b";'
+    other = 'int f(int a) {\n  return 3 * a;\n}\nconst char *s = "a//b";\n'
+    lit = 'int f(int a) {\n  return 2 * a;\n}\nconst char *s = "a/*b";\n'
+    tok = bench.code_tokens
+    assert tok(src) == tok(same)
+    assert tok(src) != tok(other)
+    assert tok(src) != tok(lit)
+    assert "//" in tok(src) and "twice" not in tok(src)
+    files = {n: src for n in bench.KERNEL_SOURCES}
+    h = bench.kernel_source_hash(files.__getitem__)
+    assert h == bench.kernel_source_hash({n: same for n in bench.KERNEL_SOURCES}.__getitem__)
+    assert h != bench.kernel_source_hash({n: other for n in bench.KERNEL_SOURCES}.__getitem__)
