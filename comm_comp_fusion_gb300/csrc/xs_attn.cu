@@ -17,7 +17,12 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
         p.n_dp = (p.n_items + G - 1) / G;
         return G;
     }
-    const int G = units < num_sms ? (int)units : num_sms;
+    // pieces of at least 16 K/V steps, but never fewer CTAs than items (or SMs)
+    const long long by_piece = units / 16, floor_g = p.n_items < num_sms ? p.n_items : num_sms;
+    long long g = by_piece > floor_g ? by_piece : floor_g;
+    if (g > num_sms) g = num_sms;
+    if (g > units) g = units;
+    const int G = (int)g;
     if (p.n_items % G == 0) {
         p.n_dp = p.n_items / G;
         return G;

@@ -45,10 +45,10 @@ def test_small_parity(case):
 # (tail waves split into pieces), and far fewer items than SMs (one item cut
 # into many pieces across many CTAs).
 BALANCED = [
-    (1, 4096, 4, 128, 2, 1.0, 128 ** -0.5),    # 64 items of 32 K/V tiles over 152 CTAs: ~3 pieces each
+    (1, 4096, 4, 128, 2, 1.0, 128 ** -0.5),    # 64 items of 32 K/V tiles over 128 CTAs: 2 pieces each
     (1, 2048, 40, 64, 4, 1.0, 1 / 8),           # 320 items: two whole waves + balanced tail
     (2, 1152, 38, 128, 2, 1.0, 128 ** -0.5),    # 380 items, lone last tiles, B = 2
-    (1, 384, 2, 128, 1, 2.0, 0.35),             # 4 items over 12 units, peaked
+    (1, 3072, 2, 128, 1, 2.0, 0.35),            # 24 items of 24 steps over 36 CTAs of 16, peaked
     (1, 256, 8, 64, 4, 1.0, 1 / 8),             # the small workload
 ]
 

@@ -73,7 +73,7 @@ CASES256 = [
     (1, 256, 8, 256, 4),     # Sl = 64 < 128
     (2, 384, 6, 256, 3),     # odd tile count, B = 2
     (1, 1024, 16, 256, 8),
-    (1, 2048, 4, 256, 2),    # few items: the balanced schedule splits every item
+    (1, 3072, 2, 256, 2),    # few items: the balanced schedule splits every item
     (1, 1000, 4, 256, 2),    # ragged S
 ]
 
