@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libxs.so")
 ROOT = os.path.dirname(PKG)
 
-SOURCES = ["xs_attn_d128.cu", "xs_attn_f8.cu", "xs_attn_d256.cu", "xs_attn_d96.cu", "xs_attn_d64.cu", "xs_attn.cu", "xs_permute.cu", "xs_api.cpp",
+SOURCES = ["xs_attn_d128.cu", "xs_attn_f8.cu", "xs_attn_d256.cu", "xs_attn_d96.cu", "xs_attn_d64.cu", "xs_attn.cu", "xs_permute.cu", "xs_api.cpp", "xs_schedule.cpp",
            "xs_noalloc.cu", "xs_burst.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,47 +1,10 @@
-// xs_attn.cu -- host side of the attention kernel: the work schedule, the
-// workspace size, dispatch to the per-head-dimension instances
-// (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu, xs_attn_d256.cu), the bounded-wait
-// self-test and the device error words.
+// xs_attn.cu -- host side of the attention kernel: the workspace size, dispatch
+// to the per-head-dimension instances (xs_attn_d64.cu, xs_attn_d96.cu,
+// xs_attn_d128.cu, xs_attn_d256.cu), the bounded-wait self-test and the device
+// error words. The work schedule is in xs_schedule.cpp.
 #include "xs_attn_kernel.cuh"
 
 namespace xs {
-
-int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
-    const long long units = (long long)p.n_items * p.n_kv;
-    p.sk_item0 = p.n_items;
-    p.sk_units = 0;
-    p.sk_q = 0;
-    p.sk_r = 0;
-    if (!balanced) {
-        const int G = p.n_items < num_sms ? p.n_items : num_sms;
-        p.n_dp = (p.n_items + G - 1) / G;
-        return G;
-    }
-    // pieces of at least 16 K/V steps, but never fewer CTAs than items (or SMs)
-    const long long by_piece = units / 16, floor_g = p.n_items < num_sms ? p.n_items : num_sms;
-    long long g = by_piece > floor_g ? by_piece : floor_g;
-    if (g > num_sms) g = num_sms;
-    if (g > units) g = units;
-    const int G = (int)g;
-    if (p.n_items % G == 0) {
-        p.n_dp = p.n_items / G;
-        return G;
-    }
-    // keep one full wave (plus the remainder) for the balanced region
-    p.n_dp = p.n_items / G - 1;
-    if (p.n_dp < 0) p.n_dp = 0;
-    p.sk_item0 = p.n_dp * G;
-    const long long u = (long long)(p.n_items - p.sk_item0) * p.n_kv;
-    if (u >= (1ll << 31)) {  // too long to split in 32-bit arithmetic: whole items only
-        p.n_dp = (p.n_items + G - 1) / G;
-        p.sk_item0 = p.n_items;
-        return G;
-    }
-    p.sk_units = (uint32_t)u;
-    p.sk_q = p.sk_units / (uint32_t)G;
-    p.sk_r = p.sk_units % (uint32_t)G;
-    return G;
-}
 
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     (void)n_kv;
