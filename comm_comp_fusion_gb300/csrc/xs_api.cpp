@@ -257,11 +257,7 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
     xs_status st = pipe_init(hp);
     if (st) return st;
     const int P = p.P, per_rank = p.n_items / P;
-    // about 8 MiB of inputs per chunk at least: a chunk's launch costs several
-    // microseconds, more than copying a small chunk takes
-    const long long by_size = (long long)((2 * qk_bytes + v_bytes) >> 23);
-    int chunks = P < kMaxChunks ? P : kMaxChunks;
-    if (by_size < chunks) chunks = by_size > 1 ? (int)by_size : 1;
+    const int chunks = xs::host_chunks(P, (long long)(2 * qk_bytes + v_bytes), kMaxChunks);
     const size_t q_rank = qk_bytes / P, v_rank = v_bytes / P, o_rank = bytes / P;
     const size_t head_row = (size_t)D * 2, pitch = (size_t)p.H * head_row;
     const char *hq = static_cast<const char *>(o.hq), *hk = static_cast<const char *>(o.hk);

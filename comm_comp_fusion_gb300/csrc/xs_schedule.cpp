@@ -1,6 +1,7 @@
 // xs_schedule.cpp -- the work schedule of an attention call: the grid size and
 // how work items are dealt to CTAs (AttnParams: n_dp, sk_item0, sk_units,
-// sk_q, sk_r). Host code only, so the CPU tests compile it on its own.
+// sk_q, sk_r), and the chunks of the host-buffer pipeline. Host code only, so
+// the CPU tests compile it on its own.
 #include "xs_internal.h"
 
 namespace xs {
@@ -40,6 +41,17 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
     p.sk_q = p.sk_units / (uint32_t)G;
     p.sk_r = p.sk_units % (uint32_t)G;
     return G;
+}
+
+// Chunks of the host-buffer pipeline: one per rank, at most max_chunks, and
+// about 8 MiB of inputs per chunk at least (a chunk's launch costs several
+// microseconds, more than copying a small chunk takes). Chunk c covers ranks
+// [c P / chunks, (c + 1) P / chunks).
+int host_chunks(int P, long long input_bytes, int max_chunks) {
+    const long long by_size = input_bytes >> 23;
+    int chunks = P < max_chunks ? P : max_chunks;
+    if (by_size < chunks) chunks = by_size > 1 ? (int)by_size : 1;
+    return chunks;
 }
 
 }  // namespace xs

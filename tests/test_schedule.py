@@ -27,6 +27,10 @@ int main() {
         xs::AttnParams p{};
         p.n_items = (int)items;
         p.n_kv = (int)nkv;
+        if (bal == 2) {  // host pipeline chunks: items = P, nkv = input bytes, sms = the cap
+            std::printf("%d\n", xs::host_chunks((int)items, nkv, sms));
+            continue;
+        }
         const int g = xs::attn_schedule(p, sms, bal != 0);
         std::printf("%d %d %d %u %u %u\n", g, p.n_dp, p.sk_item0, p.sk_units, p.sk_q, p.sk_r);
     }
@@ -111,3 +115,21 @@ def test_grid_rule_examples(schedule):
     assert got[2][:3] == (64, 1, 64) and got[2][3] == 0  # one whole item per CTA
     assert got[3][:3] == (8, 1, 8) and got[3][3] == 0
     assert got[4][:4] == (152, 2, 200, 0)                # whole items only
+
+
+def test_host_pipeline_chunks(schedule):
+    """One chunk per rank, at most 16, and at least about 8 MiB of inputs per
+    chunk: DiT (P = 8, 75.5 MB of q, k, v) takes 8 chunks, a small call one,
+    P = 32 at S = 8192 the cap of 16. Chunk c's ranks [cP/n, (c+1)P/n) cover
+    every rank once with at least one rank each."""
+    MB = 1 << 20
+    cases = [(8, 75497472, 16, 2), (4, 1 << 20, 16, 2), (32, 3 * 32 * 8192 * 128 * 2 * 4, 16, 2),
+             (8, 20 * MB, 16, 2), (1, 10 ** 9, 16, 2), (3, 0, 16, 2)]
+    got = [r[0] for r in schedule(cases)]
+    assert got == [8, 1, 16, 2, 1, 1]
+    for P in range(1, 40):
+        for inp in (0, 9 * MB, 40 * MB, 10 ** 9):
+            n = schedule([(P, inp, 16, 2)])[0][0]
+            assert 1 <= n <= min(P, 16)
+            spans = [((c + 1) * P // n) - (c * P // n) for c in range(n)]
+            assert sum(spans) == P and min(spans) >= 1
