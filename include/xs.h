@@ -157,6 +157,8 @@ xs_status xs_attn_causal(const void *q, const void *k, const void *v, void *out,
  * leaving some SMs idle: an output tile pair whose K/V range is split across
  * CTAs is computed in pieces whose partial rows (unnormalised O in fp32, row
  * max, row sum) meet in the workspace and are merged in a fixed order.
+ * Small calls run on fewer CTAs so that pieces hold at least 16 K/V tiles,
+ * but never on fewer CTAs than work items (or SMs).
  *   workspace       : device memory, 256-byte aligned, at least the size that
  *                     xs_attn_workspace_size reports for these shapes on the
  *                     current device; its contents need no initialisation and
