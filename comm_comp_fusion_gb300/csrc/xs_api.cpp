@@ -190,7 +190,10 @@ int gcd_int(int a, int b) {
     return a;
 }
 
-std::atomic<uint32_t> g_generation{1};
+// Generation stamps of balanced launches (48 bits are used; counting from 1, so
+// the zero of fresh memory never matches).
+std::atomic<unsigned long long> g_generation{1};
+unsigned long long next_generation() { return g_generation.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1ull); }
 
 // What an attention call does besides the plain head-partitioned one.
 struct CallOpts {
@@ -285,7 +288,7 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
         xs::AttnParams pc = p;
         pc.item0 = r0 * per_rank;
         pc.n_items = nr * per_rank;
-        if (pc.ws_rec) pc.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
+        if (pc.ws_rec) pc.gen = next_generation();
         const int grid = xs::attn_schedule(pc, info.num_sms, pc.ws_rec != nullptr && !o.causal);
         e = launch_any(o, D, maps, pc, grid, s);
         if (e == cudaSuccess) e = cudaEventRecord(hp.comp[c], s);
@@ -416,8 +419,8 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
         if ((st = check_device_pointer(ws, dev, "workspace"))) return st;
         const size_t rec = ((size_t)2 * info.num_sms * xs::partial_record_bytes(D) + 255) & ~(size_t)255;
         p.ws_rec = static_cast<float *>(ws);
-        p.ws_cnt = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + rec);
-        p.gen = g_generation.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFu;
+        p.ws_cnt = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + rec);
+        p.gen = next_generation();
     }
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (host) return host_pipeline(o, q, k, v, out, qk_bytes, v_bytes, bytes, D, p, head_maps, info, dev, s);

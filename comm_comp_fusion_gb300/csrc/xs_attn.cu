@@ -9,8 +9,8 @@ namespace xs {
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     (void)n_kv;
     const size_t rec = ((size_t)2 * num_sms * partial_record_bytes(D) + 255) & ~(size_t)255;
-    // four epilogue warps' arrival counters per tile
-    const size_t cnt = ((size_t)n_items * 4 * tiles_per_item(D) * sizeof(uint32_t) + 255) & ~(size_t)255;
+    // four epilogue warps' arrival counters (64-bit words) per tile
+    const size_t cnt = ((size_t)n_items * 4 * tiles_per_item(D) * sizeof(unsigned long long) + 255) & ~(size_t)255;
     return rec + cnt;
 }
 

@@ -221,20 +221,6 @@ __device__ __forceinline__ bool sched_done(const Sched &s, const AttnParams &p) 
     return !sched_next<CAU>(t, p, g);
 }
 
-// Counts an arrival on a counter stamped with this call's generation (low 12
-// bits: arrivals, high 20: generation; a stale stamp counts as zero). Returns
-// true for the n-th arrival. The CAS loop ends after at most n retries.
-__device__ __forceinline__ bool arrive_last(uint32_t *cnt, uint32_t gen, uint32_t n) {
-    gen &= 0xFFFFFu;
-    uint32_t old = *reinterpret_cast<volatile uint32_t *>(cnt);
-    for (;;) {
-        const uint32_t cur = (old >> 12) == gen ? (old & 0xFFFu) : 0u;
-        const uint32_t prev = atomicCAS(cnt, old, (gen << 12) | (cur + 1u));
-        if (prev == old) return cur + 1u == n;
-        old = prev;
-    }
-}
-
 __device__ __forceinline__ float ld_cg(const float *ptr) {
     float v;
     asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
@@ -413,12 +399,9 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
     using R = Rec<D>;
     const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
     const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
-    uint32_t *cnt = p.ws_cnt + ((size_t)x_local * 4 + wq);
+    const unsigned long long *cnt = p.ws_cnt + ((size_t)x_local * 4 + wq);
     uint32_t others = 0;
-    if (lane == 0) {
-        const uint32_t v = *reinterpret_cast<volatile uint32_t *>(cnt);
-        others = ((v >> 12) == (p.gen & 0xFFFFFu) && (v & 0xFFFu) == npieces - 1u) ? 1u : 0u;
-    }
+    if (lane == 0) others = arrivals_now(cnt, p.gen) == npieces - 1u ? 1u : 0u;
     others = __shfl_sync(0xffffffffu, others, 0);
     if (others) {
         __threadfence();

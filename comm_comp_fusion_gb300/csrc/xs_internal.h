@@ -35,8 +35,8 @@ struct AttnParams {
     uint32_t sk_units;     // units U in the balanced region (0: none), below 2^31
     uint32_t sk_q, sk_r;   // U = sk_q * G + sk_r, so range starts are c*q + (c*r)/G
     float *ws_rec;         // 2 * G partial records (see partial_record_bytes)
-    uint32_t *ws_cnt;      // 8 arrival counters per item of the balanced region
-    uint32_t gen;          // generation stamped into the counters by this call
+    unsigned long long *ws_cnt;  // arrival counters, 4 per tile of each item of the balanced region
+    unsigned long long gen;      // this launch's 48-bit generation, stamped into the counters
     unsigned long long *trace;  // traced instances: epilogue records, kTraceWords per (CTA, item, tile, warp)
 };
 

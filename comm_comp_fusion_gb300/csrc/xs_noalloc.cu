@@ -15,8 +15,11 @@
 //   * every call on a device uses the same array, which keeps the previous
 //     call's contents; calls that may overlap on the GPU (different streams,
 //     no ordering between them) race on it and must not be issued;
-//   * the arrival counters are cleared (cudaMemsetAsync on the calling stream)
-//     before every launch; the partial rows need no clearing;
+//   * nothing in the array has to start at zero: the partial rows are written
+//     before they are read, and each arrival counter carries the 48-bit
+//     generation of the launch that wrote it, so a count left by an earlier
+//     call reads as zero. A call therefore writes the array only from its
+//     kernel, after every argument check has passed;
 //   * the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current, so that first call
 //     should come before any stream capture;
@@ -38,7 +41,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 struct ScratchState {
     bool ready = false;
     unsigned char *ptr = nullptr;  // device address of g_noalloc_scratch on this device
-    int num_sms = 0;
 };
 ScratchState g_state[kMaxDevices];
 std::mutex g_mu;
@@ -55,8 +57,6 @@ xs_status scratch_for_current_device(ScratchState *out) {
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || ptr == nullptr)
             return (xs_status)xs::report_error(XS_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed");
-        e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return (xs_status)xs::report_error(XS_ERR_CUDA, "cudaDeviceGetAttribute failed");
         s.ptr = static_cast<unsigned char *>(ptr);
         s.ready = true;
     }
@@ -85,9 +85,6 @@ extern "C" xs_status xs_attn_a2a_noalloc(const void *q, const void *k, const voi
         return (xs_status)xs::report_error(XS_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
     ScratchState s;
     if ((st = scratch_for_current_device(&s)) != XS_OK) return st;
-    // clear the arrival counters, which follow the partial records
-    const size_t rec = ((size_t)2 * s.num_sms * xs::partial_record_bytes(D) + 255) & ~(size_t)255;
-    cudaError_t e = cudaMemsetAsync(s.ptr + rec, 0, need - rec, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return (xs_status)xs::report_error(XS_ERR_CUDA, "clearing the scratch counters failed");
+    // xs_attn_a2a_ws checks every remaining argument before it enqueues anything
     return xs_attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, s.ptr, kScratchBytes, stream);
 }

@@ -332,4 +332,29 @@ template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------------------ split-item arrival counters
+
+// A counter word of a split item is (generation << 16) | arrivals, where the
+// generation is the calling launch's 48-bit stamp (a process-wide count of
+// balanced launches, so it does not repeat within 2^48 launches). A word that
+// carries another generation, such as one left by an earlier call or the zero of
+// fresh memory, counts as no arrivals, so the workspace never needs clearing.
+constexpr unsigned long long kGenMask = (1ull << 48) - 1ull;
+__device__ __forceinline__ uint32_t arrivals_now(const unsigned long long *cnt, unsigned long long gen) {
+    const unsigned long long w = *reinterpret_cast<const volatile unsigned long long *>(cnt);
+    return (w >> 16) == (gen & kGenMask) ? (uint32_t)(w & 0xFFFFull) : 0u;
+}
+// Counts one arrival and returns true for the n-th. The CAS loop ends after at
+// most n retries (each failure means another arrival got in first).
+__device__ __forceinline__ bool arrive_last(unsigned long long *cnt, unsigned long long gen, uint32_t n) {
+    gen &= kGenMask;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(cnt);
+    for (;;) {
+        const unsigned long long cur = (old >> 16) == gen ? (old & 0xFFFFull) : 0ull;
+        const unsigned long long prev = atomicCAS(cnt, old, (gen << 16) | (cur + 1ull));
+        if (prev == old) return cur + 1ull == (unsigned long long)n;
+        old = prev;
+    }
+}
+
 }  // namespace xs

@@ -194,8 +194,10 @@ xs_status xs_attn_workspace_size(int B, int S, int H, int D, int P, size_t *byte
  *     with XS_ERR_WORKSPACE before anything is enqueued
  *     (xs_attn_workspace_size reports the need).
  *   - Every call on a device shares the one scratch area, which keeps the
- *     previous call's contents; its counters are cleared on the calling stream
- *     before each launch. Calls that may overlap on the GPU race on the scratch
+ *     previous call's contents. Nothing in it needs clearing: partial rows are
+ *     written before they are read, and the arrival counters carry a per-launch
+ *     generation stamp. Only the kernel of a call that passed every argument
+ *     check writes it. Calls that may overlap on the GPU race on the scratch
  *     area and must not be issued.
  *   - The first call on a device looks up the scratch area's device address
  *     with that device current; make that first call before any stream capture.

@@ -21,6 +21,16 @@ def _has_gpu():
         return False
 
 
+@pytest.fixture(autouse=True)
+def _guard_bands(request):
+    """After every GPU test: the guard bands of every guarded buffer it
+    allocated (xs_testlib.guarded) must be intact."""
+    yield
+    if "gpu" in request.keywords and _has_gpu():
+        import xs_testlib
+        xs_testlib.check_guards()
+
+
 def pytest_collection_modifyitems(config, items):
     if _has_gpu():
         return

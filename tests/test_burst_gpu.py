@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import xsgen
-from xs_testlib import from_dev, to_dev
+from xs_testlib import guarded, from_dev, to_dev
 
 
 @pytest.mark.gpu
@@ -19,8 +19,8 @@ def test_burst_records(isolated):
     import torch
     import comm_comp_fusion_gb300 as xs
     K, B, n, gap = 16, 8192, 12, 2000.0
-    buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
-    rec = torch.empty(xs.burst_rec_bytes(K, n), dtype=torch.uint8, device="cuda")
+    buf = guarded(64 << 20, torch.uint8)
+    rec = guarded(xs.burst_rec_bytes(K, n), torch.uint8)
     s = xs.burst_gap(buf, buf.numel(), rec, rec.numel(), K, B, gap, n, isolated, 128, 6144)
     assert 500.0 < s["sm_clock_mhz"] < 3500.0
     assert 0.0 < s["t_iss_mean_ns"] <= s["t_iss_max_ns"] < 1e6
@@ -39,8 +39,8 @@ def test_burst_gap_lengthens_period():
     import torch
     import comm_comp_fusion_gb300 as xs
     K, B, n = 32, 16384, 24
-    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    rec = torch.empty(xs.burst_rec_bytes(K, n), dtype=torch.uint8, device="cuda")
+    buf = guarded(256 << 20, torch.uint8)
+    rec = guarded(xs.burst_rec_bytes(K, n), torch.uint8)
     p = [xs.burst_gap(buf, buf.numel(), rec, rec.numel(), K, B, g, n)["t_period_ns"] for g in (10000.0, 20000.0)]
     assert 0.8 * 10000.0 < p[1] - p[0] < 1.2 * 10000.0
 
@@ -49,7 +49,7 @@ def test_burst_gap_lengthens_period():
 def test_burst_rejects():
     import torch
     import comm_comp_fusion_gb300 as xs
-    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    buf = guarded(1 << 20, torch.uint8)
     rec = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(xs.XsError):
         xs.burst_gap(buf, buf.numel(), rec, rec.numel(), 4, 3000, 0.0, 4)     # B not a multiple of 512 * warps
@@ -70,11 +70,11 @@ def test_trace_matches_untraced_and_covers_tiles(case):
     B, S, H, D, P = case
     scale = D ** -0.5
     q, k, v = (to_dev(a) for a in xsgen.random_inputs(900 + S + H, P, B, S, H, D))
-    ref = torch.full_like(q, -1)
-    out = torch.full_like(q, -1)
+    ref = guarded(q.numel())
+    out = guarded(q.numel())
     xs.attn_a2a(q, k, v, ref, B, S, H, D, P, scale)
     ctas, per, nb = xs.trace_layout(B, S, H, D, P)
-    tr = torch.full((nb // 8,), -1, dtype=torch.int64, device="cuda")
+    tr = guarded(nb // 8, torch.int64, -1)
     xs.attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, tr, nb)
     torch.cuda.synchronize()
     assert xs.device_status() == xs.XS_OK

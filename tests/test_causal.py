@@ -9,7 +9,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
 
 
 def run_causal(q, k, v, B, S, H, D, P, scale):
@@ -17,7 +17,7 @@ def run_causal(q, k, v, B, S, H, D, P, scale):
     import comm_comp_fusion_gb300 as xs
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     n = q.size
-    fused, head, serial = (torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(3))
+    fused, head, serial = (guarded(n) for _ in range(3))
     xs.attn_causal_a2a(tq, tk, tv, fused, B, S, H, D, P, scale)
     xs.attn_causal(tq, tk, tv, head, B, S, H, D, P, scale)
     xs.a2a_permute(head, serial, B, S, H, D, P)
@@ -69,7 +69,7 @@ def test_causal_differs_from_full():
     B, S, H, D, P = 1, 512, 2, 128, 1
     q, k, v = xsgen.random_inputs(11, P, B, S, H, D)
     _, head, _ = run_causal(q, k, v, B, S, H, D, P, D ** -0.5)
-    full = torch.full((q.size,), -1, dtype=torch.int16, device="cuda")
+    full = guarded(q.size)
     xs.attn(to_dev(q), to_dev(k), to_dev(v), full, B, S, H, D, P, D ** -0.5)
     torch.cuda.synchronize()
     f = from_dev(full).reshape(S, H, D)

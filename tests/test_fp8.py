@@ -11,7 +11,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
 
 D = 128
 
@@ -37,11 +37,11 @@ def run_q8(q8, k8, v, B, S, H, P, scale, balanced):
     ws, nb = None, 0
     if balanced:
         nb = xs.workspace_size(B, S, H, D, P)
-        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+        ws = guarded(max(nb, 256), torch.uint8)
         ws.fill_(0xA5)
-    fused = torch.full((n,), -1, dtype=torch.int16, device="cuda")
-    head = torch.full_like(fused, -1)
-    serial = torch.full_like(fused, -1)
+    fused = guarded(n)
+    head = guarded(fused.numel())
+    serial = guarded(fused.numel())
     fused_fn(tq, tk, tv, fused, B, S, H, D, P, scale, ws, nb)
     head_fn(tq, tk, tv, head, B, S, H, D, P, scale, ws, nb)
     xs.a2a_permute(head, serial, B, S, H, D, P)
@@ -107,7 +107,7 @@ def test_q8_matches_bf16_kernel_on_widened_inputs():
     qb = xsgen.f32_to_bf16_bits(oracle.e4m3_decode(q8).astype(np.float32))
     kb = xsgen.f32_to_bf16_bits(oracle.e4m3_decode(k8).astype(np.float32))
     _, head8, _ = run_q8(q8, k8, v, B, S, H, P, scale, False)
-    out = torch.full((q8.size,), -1, dtype=torch.int16, device="cuda")
+    out = guarded(q8.size)
     xs.attn(to_dev(qb), to_dev(kb), to_dev(v), out, B, S, H, D, P, scale)
     torch.cuda.synchronize()
     a = xsgen.bf16_bits_to_f32(head8).astype(np.float64)

@@ -8,7 +8,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, run_paths, run_paths_ws, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, run_paths, run_paths_ws, to_dev
 
 CASES = [
     (1, 256, 8, 96, 4),     # the small workload's layout, Sl = 64
@@ -42,8 +42,8 @@ def test_d96_permutes_bit_exact(case):
     import comm_comp_fusion_gb300 as xs
     B, S, H, D, P = case
     x = xsgen.normal_bf16(55 + S, 7, (P, B, S, H // P, D))
-    seq = torch.full((x.size,), -1, dtype=torch.int16, device="cuda")
-    back = torch.full_like(seq, -1)
+    seq = guarded(x.size)
+    back = guarded(seq.numel())
     xs.a2a_permute(to_dev(x), seq, B, S, H, D, P)
     xs.a2a_permute_inverse(seq, back, B, S, H, D, P)
     torch.cuda.synchronize()
@@ -58,7 +58,7 @@ def test_d96_ulysses():
     B, S, H, D, P = 1, 1024, 8, 96, 8
     shape = (P, B, S // P, H, D)
     q, k, v = (xsgen.normal_bf16(77, i, shape) for i in (1, 2, 3))
-    out = torch.full((q.size,), -1, dtype=torch.int16, device="cuda")
+    out = guarded(q.size)
     xs.ulysses_attn(to_dev(q), to_dev(k), to_dev(v), out, B, S, H, D, P, D ** -0.5)
     torch.cuda.synchronize()
     got = from_dev(out)
@@ -102,7 +102,7 @@ def test_d256_causal_and_ulysses():
     scale = D ** -0.5
     q, k, v = xsgen.random_inputs(61, P, B, S, H, D)
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
-    out = torch.full((q.size,), -1, dtype=torch.int16, device="cuda")
+    out = guarded(q.size)
     xs.attn_causal_a2a(tq, tk, tv, out, B, S, H, D, P, scale)
     torch.cuda.synchronize()
     ref = oracle.attention(q, k, v, B, S, H, D, P, scale, causal=True)
@@ -110,7 +110,7 @@ def test_d256_causal_and_ulysses():
     # both All-to-Alls fused: inputs read as sequence-partitioned
     shape = (P, B, S // P, H, D)
     qs, ks, vs = (xsgen.normal_bf16(62, i, shape) for i in (1, 2, 3))
-    out2 = torch.full((qs.size,), -1, dtype=torch.int16, device="cuda")
+    out2 = guarded(qs.size)
     xs.ulysses_attn(to_dev(qs), to_dev(ks), to_dev(vs), out2, B, S, H, D, P, scale)
     torch.cuda.synchronize()
     hq, hk, hv = (oracle.a2a_inverse(x, B, S, H, D, P) for x in (qs, ks, vs))
@@ -123,8 +123,8 @@ def test_d256_permute_bit_exact():
     import comm_comp_fusion_gb300 as xs
     B, S, H, D, P = 2, 96, 8, 256, 4
     x = xsgen.normal_bf16(63, 7, (P, B, S, H // P, D))
-    seq = torch.full((x.size,), -1, dtype=torch.int16, device="cuda")
-    back = torch.full_like(seq, -1)
+    seq = guarded(x.size)
+    back = guarded(seq.numel())
     xs.a2a_permute(to_dev(x), seq, B, S, H, D, P)
     xs.a2a_permute_inverse(seq, back, B, S, H, D, P)
     torch.cuda.synchronize()

@@ -8,7 +8,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, to_dev
 
 CASES = [
     (1, 1024, 16, 128, 8),   # small: one chunk
@@ -38,12 +38,12 @@ def _run(q, k, v, B, S, H, D, P, scale, balanced, pinned, fused=True):
     hq, hk, hv = (_host(a, pinned) for a in (q, k, v))
     hout = torch.full((n,), -1, dtype=torch.int16)
     hout = hout.pin_memory() if pinned else hout
-    dq, dk, dv = (torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(3))
-    dout = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    dq, dk, dv = (guarded(n) for _ in range(3))
+    dout = guarded(n)
     ws, nb = None, 0
     if balanced:
         nb = xs.workspace_size(B, S, H, D, P)
-        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+        ws = guarded(max(nb, 256), torch.uint8)
     fn = xs.attn_a2a_host if fused else xs.attn_host
     fn(hq, hk, hv, hout, dq, dk, dv, dout, B, S, H, D, P, scale, ws, nb)
     torch.cuda.synchronize()
@@ -62,8 +62,8 @@ def test_host_whole_items_bit_exact(case):
     B, S, H, D, P = case
     scale = D ** -0.5
     q, k, v = xsgen.random_inputs(31 + S + H + P, P, B, S, H, D)
-    ref_f = torch.full((q.size,), -1, dtype=torch.int16, device="cuda")
-    ref_h = torch.full_like(ref_f, -1)
+    ref_f = guarded(q.size)
+    ref_h = guarded(ref_f.numel())
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     xs.attn_a2a(tq, tk, tv, ref_f, B, S, H, D, P, scale)
     xs.attn(tq, tk, tv, ref_h, B, S, H, D, P, scale)
@@ -101,12 +101,12 @@ def test_host_back_to_back_calls_keep_order():
     ins = [xsgen.random_inputs(s, P, B, S, H, D) for s in (5, 6)]
     hin = [[_host(a, True) for a in x] for x in ins]
     houts = [torch.empty(ins[0][0].size, dtype=torch.int16).pin_memory() for _ in range(2)]
-    dq, dk, dv, dout = (torch.empty(ins[0][0].size, dtype=torch.int16, device="cuda") for _ in range(4))
+    dq, dk, dv, dout = (guarded(ins[0][0].size) for _ in range(4))
     for (hq, hk, hv), ho in zip(hin, houts):
         xs.attn_a2a_host(hq, hk, hv, ho, dq, dk, dv, dout, B, S, H, D, P, scale)
     torch.cuda.synchronize()
     for (q, k, v), ho in zip(ins, houts):
-        ref = torch.empty_like(dout)
+        ref = guarded(dout.numel())
         xs.attn_a2a(to_dev(q), to_dev(k), to_dev(v), ref, B, S, H, D, P, scale)
         torch.cuda.synchronize()
         assert np.array_equal(ho.numpy().view(np.uint16), from_dev(ref))

@@ -9,7 +9,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, sample_rows, seq_rows_of, to_dev
 
 CASES = [
     (1, 131072, 4, 128, 2, False),
@@ -38,10 +38,10 @@ def test_long_sequence_sampled(case):
     tv = to_dev(v)
     n = v.size
     nb = xs.workspace_size(B, S, H, D, P)
-    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
-    fused = torch.full((n,), -1, dtype=torch.int16, device="cuda")
-    head = torch.full_like(fused, -1)
-    serial = torch.full_like(fused, -1)
+    ws = guarded(max(nb, 256), torch.uint8)
+    fused = guarded(n)
+    head = guarded(fused.numel())
+    serial = guarded(fused.numel())
     if q8:
         xs.attn_a2a_q8(tq, tk, tv, fused, B, S, H, D, P, scale, ws, nb)
         xs.attn_q8(tq, tk, tv, head, B, S, H, D, P, scale, ws, nb)

@@ -9,7 +9,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, to_dev
 
 
 def _shapes(n, seed):
@@ -33,7 +33,7 @@ CASES = _shapes(24, 2026)
 
 def _buf(n):
     import torch
-    return torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    return guarded(n)
 
 
 @pytest.mark.gpu
@@ -47,7 +47,7 @@ def test_matrix(case):
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     n = q.size
     nb = xs.workspace_size(B, S, H, D, P)
-    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    ws = guarded(max(nb, 256), torch.uint8)
     fused_ws, head_ws, fused, head, perm = (_buf(n) for _ in range(5))
     xs.attn_a2a_ws(tq, tk, tv, fused_ws, B, S, H, D, P, scale, ws, nb)
     xs.attn_ws(tq, tk, tv, head_ws, B, S, H, D, P, scale, ws, nb)

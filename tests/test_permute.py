@@ -5,7 +5,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import from_dev, to_dev
+from xs_testlib import guarded, from_dev, to_dev
 
 SHAPES = [  # (B, S, H, D, P)
     (1, 256, 8, 64, 4),      # the small workload
@@ -26,7 +26,7 @@ def test_permute_matches_oracle(shape):
     B, S, H, D, P = shape
     n = B * S * H * D
     x = np.random.default_rng(n).integers(0, 1 << 16, n, dtype=np.uint16).reshape(P, B, S, H // P, D)
-    out = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    out = guarded(n)
     xs.a2a_permute(to_dev(x), out, B, S, H, D, P)
     torch.cuda.synchronize()
     assert np.array_equal(from_dev(out).reshape(P, B, S // P, H, D), oracle.a2a(x, B, S, H, D, P))
@@ -40,7 +40,7 @@ def test_permute_round_trip_and_stream():
     x = xsgen.normal_bf16(5, 1, (P, B, S, H // P, D))
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        out = torch.empty(x.size, dtype=torch.int16, device="cuda")
+        out = guarded(x.size)
         xs.a2a_permute(to_dev(x), out, B, S, H, D, P, stream=s)
     s.synchronize()
     y = from_dev(out).reshape(P, B, S // P, H, D)

@@ -18,7 +18,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, run_paths, run_paths_ws, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, run_paths, run_paths_ws, to_dev
 
 CASES = [  # (B, S, H, D, P)
     (1, 2048, 4, 128, 2),
@@ -89,7 +89,7 @@ def test_ramp_parity_causal(case):
     scale = D ** -0.5
     q, k, v = ramped_inputs(610 + S, B, S, H, D, P)
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
-    out = torch.full_like(tq, -1)
+    out = guarded(tq.numel())
     xs.attn_causal_a2a(tq, tk, tv, out, B, S, H, D, P, scale)
     torch.cuda.synchronize()
     assert xs.device_status() == xs.XS_OK, xs.last_error()

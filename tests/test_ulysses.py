@@ -14,7 +14,7 @@ import pytest
 import oracle
 import xsgen
 
-from xs_testlib import SENTINEL, assert_close, from_dev, to_dev
+from xs_testlib import guarded, SENTINEL, assert_close, from_dev, to_dev
 
 
 def seq_inputs(seed, B, S, H, D, P, sigma_qk=1.0, sigma_v=1.0):
@@ -33,11 +33,11 @@ def run_ulysses(q, k, v, B, S, H, D, P, scale):
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     n = q.size
     nb = xs.workspace_size(B, S, H, D, P)
-    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
-    outs = [torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(4)]
+    ws = guarded(max(nb, 256), torch.uint8)
+    outs = [guarded(n) for _ in range(4)]
     xs.ulysses_attn(tq, tk, tv, outs[0], B, S, H, D, P, scale, ws, nb)
     xs.ulysses_attn(tq, tk, tv, outs[1], B, S, H, D, P, scale)
-    hq, hk, hv = (torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in range(3))
+    hq, hk, hv = (guarded(n) for _ in range(3))
     for src, dst in ((tq, hq), (tk, hk), (tv, hv)):
         xs.a2a_permute_inverse(src, dst, B, S, H, D, P)
     xs.attn_a2a_ws(hq, hk, hv, outs[2], B, S, H, D, P, scale, ws, nb)
@@ -67,8 +67,8 @@ def test_inverse_permute_bit_exact(case):
     B, S, H, D, P = case
     x = xsgen.normal_bf16(77 + S + H, 5, (P, B, S // P, H, D))
     tx = to_dev(x)
-    head = torch.full((x.size,), -1, dtype=torch.int16, device="cuda")
-    back = torch.full_like(head, -1)
+    head = guarded(x.size)
+    back = guarded(head.numel())
     xs.a2a_permute_inverse(tx, head, B, S, H, D, P)
     xs.a2a_permute(head, back, B, S, H, D, P)
     torch.cuda.synchronize()
