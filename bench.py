@@ -1,28 +1,33 @@
 """Benchmark of the fused attention + All-to-All scatter on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+    python bench.py --sweep-m [--lengths 8192,16384,...] [--reps N] [--json PATH]
 
-A step is one xs_attn_a2a call (every step of the hot path: Q/K/V tile loads,
-QK^T, online softmax, PV, normalisation and the scatter of each output tile
-into its rank slice) over one batch of the synthetic workload. The default
-workload is the DiT-style one (B=1, S=4096, H=24, D=128, P=8); the inputs
-(PCG32 -> Box-Muller -> bf16, seed 1000 + workload index) are resident in HBM
-before timing starts. Each timed launch is preceded by a 512 MiB write that
-flushes the 129 MB L2, and timed by CUDA events recorded on the launch stream
-around that launch alone; W untimed warm-up steps come first, and the timed
-region is bracketed by a barrier and torch.cuda.synchronize().
+A step is one xs_attn_a2a_ws call (every step of the hot path: Q/K/V tile
+loads, QK^T, online softmax, PV, normalisation and the scatter of each output
+tile into its rank slice) over one batch of the synthetic workload. The default
+workload is the largest: B=2, S=16384, H=40, D=128, P=4 with Q, K ~ N(0, 2)
+(peaked softmax). The inputs (PCG32 -> Box-Muller -> bf16, seed 1000 + workload
+index) are resident in HBM before timing starts. Each timed launch is preceded
+by a 512 MiB write that flushes the 129 MB L2, and timed by CUDA events
+recorded on the launch stream around that launch alone; W untimed warm-up steps
+come first, and the timed region is bracketed by a barrier and
+torch.cuda.synchronize().
 
-The line also reports, from a second timed region in the same run, the
-attention-only time, the serial composition (attention, then the standalone
-permute) and the permute alone, from which the overhead of the fused scatter
-over attention alone (E_res), the hiding ratio H and the speedup over serial
-follow (X-Stage paper, arXiv 2607.23264v1, section 5.3, Eq. 21). A third
-region times ``xs_ulysses_attn`` (both Ulysses All-to-Alls fused: Q, K, V read
-from and O written to the sequence partition) against the post-only fused call
-and against its serial composition (three pre-attention permutes, attention,
-the post-attention permute); it is reported under ``ulysses``. ``e2e``
-times the same call with the inputs copied in from pinned host memory and the
-output copied back inside the timed region.
+The line also reports, from further timed regions of the same run:
+  * the comparison of the X-Stage paper (arXiv 2607.23264v1), section 5.3:
+    attention only, the serial composition (attention, then the standalone
+    permute) and the permute alone, from which the overhead of the fused
+    scatter over attention alone (E_res), the hiding ratio H (Eq. 21) and the
+    speedup over serial follow; ``per_config`` repeats it on each of the five
+    synthetic configurations;
+  * ``ulysses``: ``xs_ulysses_attn`` (both Ulysses All-to-Alls fused) against
+    the post-only fused call and its serial composition;
+  * ``sustained``: the timed call launched back to back for a few seconds;
+  * ``epilogue``: the per-tile store spans of the fused epilogue, from the
+    traced call (section 5.2.3's instrumentation);
+  * ``e2e``: the same call with the inputs copied in from pinned host memory
+    and the output copied back inside the timed region.
 
 --q8 times the E4M3 query/key call (xs_attn_a2a_q8) on the same draws
 rounded to E4M3; v and the output stay bf16. --qkv8 times the call with E4M3
@@ -31,6 +36,9 @@ values as well (xs_attn_a2a_qkv8).
 --impl reference times the fp64 CPU oracle (the checker of this library, not
 a tuned CPU implementation) on the host cores over a bounded sample of query
 rows of the same workload; it runs on rank 0 only.
+
+--sweep-m prints FA-only, Serial and Fused over the full sequence length M in
+the structure of the paper's Table 3 (section 5.3) instead of the bench line.
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload on its
 own GPU ("replicas only": the simulated All-to-All never leaves a GPU); the
@@ -297,6 +305,134 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- GPU leg
 
+def _torch_dev(a, dev):
+    import numpy as np
+    import torch
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+
+def timed(fns, steps, flush, stream, dev):
+    """Per-launch CUDA-event times (ms) of each fn, the L2 flushed before each
+    launch, the order rotated every step so that clock drift hits every fn alike."""
+    import torch
+    ev = {i: [] for i in range(len(fns))}
+    for s in range(steps):
+        order = list(range(len(fns)))
+        order = order[s % len(order):] + order[:s % len(order)]
+        for i in order:
+            flush.fill_(s & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fns[i]()
+            e1.record(stream)
+            ev[i].append((e0, e1))
+    torch.cuda.synchronize(dev)
+    return [[a.elapsed_time(b) for a, b in ev[i]] for i in range(len(fns))]
+
+
+def comparison_entry(w, flops, nbytes, peaks, t_fused, t_attn, t_serial, t_perm, t_whole):
+    """One workload's line of the section 5.3 comparison (medians, µs)."""
+    med = lambda xs_: 1e3 * statistics.median(xs_)
+    tf, ta, ts, tp, tw = (med(t) for t in (t_fused, t_attn, t_serial, t_perm, t_whole))
+    e_res = tf - ta
+    tflops = flops / (tf * 1e-6) / 1e12
+    return {
+        "workload": w["name"], "flop": flops,
+        "t_fused_us": tf, "tflops": tflops, "frac": tflops / peaks["bf16_tflops"],
+        "frac_sustained_peak": tflops / peaks["bf16_tflops_sustained"],
+        "t_attn_us": ta, "e_res_us": e_res, "e_res_pct_of_attn": 100.0 * e_res / ta,
+        "t_serial_us": ts, "speedup_vs_serial": ts / tf,
+        "hiding_ratio": (1.0 - e_res / (ts - ta)) if ts > ta else None,
+        "t_fused_whole_items_us": tw,
+        "permute": {"t_us": tp, "gbs": 2 * nbytes / (tp * 1e-6) / 1e9,
+                    "frac_hbm": 2 * nbytes / (tp * 1e-6) / 1e9 / peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
+    }
+
+
+def measure_config(idx, steps, warmup, flush, stream, dev, peaks):
+    """The section 5.3 comparison on workload idx (bf16, non-causal): the balanced
+    fused call, attention only, serial (attention then permute), the permute and
+    the whole-item fused call, interleaved; medians."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    import xsgen
+    w = xsgen.WORKLOADS[idx]
+    B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
+    q, k, v = (_torch_dev(a, dev) for a in xsgen.workload_inputs(idx))
+    out, head, serial, whole = (torch.empty_like(q) for _ in range(4))
+    nb = xs.workspace_size(B, S, H, D, P)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+    fused = lambda: xs.attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, ws, nb, stream=sp)
+    attn = lambda: xs.attn_ws(q, k, v, head, B, S, H, D, P, scale, ws, nb, stream=sp)
+    perm = lambda: xs.a2a_permute(head, serial, B, S, H, D, P, stream=sp)
+    fused_whole = lambda: xs.attn_a2a(q, k, v, whole, B, S, H, D, P, scale, stream=sp)
+
+    def serial_fn():
+        attn()
+        perm()
+
+    fns = [fused, attn, serial_fn, perm, fused_whole]
+    for _ in range(warmup):
+        for f in fns:
+            f()
+    torch.cuda.synchronize(dev)
+    t = timed(fns, steps, flush, stream, dev)
+    assert xs.device_status(sp) == xs.XS_OK, xs.last_error()
+    entry = comparison_entry(w, workload_flops(w), workload_bytes(w), peaks, *t)
+    del q, k, v, out, head, serial, whole, ws
+    torch.cuda.empty_cache()
+    return entry
+
+
+def epilogue_spans(xs, q, k, v, out, w, flush, stream, dev, sm_mhz, hbm_gbs):
+    """Per-tile store spans of the fused epilogue from the traced call (whole-item
+    schedule; the paper's per-tile store-span instrumentation, section 5.2.3):
+    for every output tile, from the first epilogue warp's first store to the last
+    warp's last store issued (clock64 of that CTA). Returns the store figures."""
+    import numpy as np
+    import torch
+    B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
+    ctas, ipc, tbytes = xs.trace_layout(B, S, H, D, P)
+    trace = torch.zeros(tbytes // 8, dtype=torch.int64, device=dev)
+    sp = stream.cuda_stream
+    xs.attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, trace, tbytes, stream=sp)
+    flush.fill_(7)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    xs.attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, trace, tbytes, stream=sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert xs.device_status(sp) == xs.XS_OK, xs.last_error()
+    t_kernel_us = 1e3 * e0.elapsed_time(e1)
+    rec = trace.cpu().numpy().view(np.uint64)[:ctas * ipc * 2 * 4 * 5].reshape(ctas, ipc, 2, 4, 5).astype(np.int64)
+    present = (rec[..., 2] > 0).all(axis=-1) & ((rec[..., 4] & 8) == 0).all(axis=-1)   # [cta][item][tile]
+    first_store = rec[..., 1].min(axis=-1)
+    last_issued = rec[..., 2].max(axis=-1)
+    ready = rec[..., 0].min(axis=-1)
+    span_cyc = (last_issued - first_store)[present].astype(np.float64)
+    lead_cyc = (first_store - ready)[present].astype(np.float64)
+    tiles = int(present.sum())
+    tile_bytes = 128 * D * 2
+    mhz = sm_mhz or 2070.0
+    span_s = span_cyc.sum() / (mhz * 1e6)
+    per_cta = tiles * tile_bytes / span_s / 1e9 if span_s > 0 else None
+    return {
+        "call": "xs_attn_a2a_trace (whole-item schedule, clock64 per tile and epilogue warp)",
+        "tiles": tiles, "bytes_per_tile": tile_bytes, "bytes_total": tiles * tile_bytes,
+        "span_us_median": float(np.median(span_cyc)) / mhz if tiles else None,
+        "span_us_p90": float(np.percentile(span_cyc, 90)) / mhz if tiles else None,
+        "ready_to_first_store_us_median": float(np.median(lead_cyc)) / mhz if tiles else None,
+        "gbs_per_cta": per_cta,
+        "gbs_all_ctas": per_cta * ctas if per_cta else None,
+        "frac_hbm_all_ctas": per_cta * ctas / hbm_gbs if per_cta else None,
+        "store_time_share": (span_s / ctas) / (t_kernel_us * 1e-6) if t_kernel_us > 0 else None,
+        "ctas": ctas, "t_traced_kernel_us": t_kernel_us, "clock_mhz_used": mhz,
+        "what": ("gbs_per_cta = all tiles' bytes / summed store spans (the rate one CTA's epilogue issues "
+                 "stores at); gbs_all_ctas = that x CTAs; store_time_share = mean per-CTA store time / kernel time"),
+    }
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -314,6 +450,7 @@ def run_ours(args):
     import comm_comp_fusion_gb300 as xs
     import xsgen
 
+    peaks, peak_src = load_peaks()
     w = xsgen.WORKLOADS[args.workload]
     B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
     nbytes = workload_bytes(w)
@@ -323,8 +460,7 @@ def run_ours(args):
         q_h, k_h = e4m3_inputs(q_h), e4m3_inputs(k_h)
     if args.v8:
         v_h = e4m3_inputs(v_h)
-    as_dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
-    q, k, v = as_dev(q_h), as_dev(k_h), as_dev(v_h)
+    q, k, v = (_torch_dev(a, dev) for a in (q_h, k_h, v_h))
     qk_bytes = nbytes // 2 if args.q8 else nbytes
     v_bytes = nbytes // 2 if args.v8 else nbytes
     out = torch.empty(nbytes // 2, dtype=torch.int16, device=dev)
@@ -385,22 +521,6 @@ def run_ours(args):
         xs.attn_ws(hq, hk, hv, head, B, S, H, D, P, scale, ws, ws_bytes, stream=sptr)
         perm()
 
-    def timed(fns, steps):
-        """Per-launch CUDA-event times (ms) of each fn, L2 flushed before each, order rotated."""
-        ev = {i: [] for i in range(len(fns))}
-        for s in range(steps):
-            order = list(range(len(fns)))
-            order = order[s % len(order):] + order[:s % len(order)]
-            for i in order:
-                flush.fill_(s & 0xFF)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fns[i]()
-                e1.record(stream)
-                ev[i].append((e0, e1))
-        torch.cuda.synchronize(dev)
-        return [[a.elapsed_time(b) for a, b in ev[i]] for i in range(len(fns))]
-
     # warm-up (also builds the per-device state of the library)
     for _ in range(args.warmup):
         fused()
@@ -419,7 +539,7 @@ def run_ours(args):
     # ---- main timed region: K fused steps
     barrier(world)
     torch.cuda.synchronize(dev)
-    t_fused = timed([fused], args.steps)[0]
+    t_fused = timed([fused], args.steps, flush, stream, dev)[0]
     torch.cuda.synchronize(dev)
     barrier(world)
     gpu_launches = args.steps  # one attention kernel per step
@@ -431,14 +551,40 @@ def run_ours(args):
     # ---- comparison region, interleaved and rotated so that clock drift hits
     # every variant alike: fused, attention only, serial (attention + permute),
     # permute only, and the whole-item fused call
-    t_fused_cmp, t_attn, t_serial, t_perm, t_whole = timed([fused, attn, serial_fn, perm, fused_whole], args.steps)
+    t_cmp = timed([fused, attn, serial_fn, perm, fused_whole], args.steps, flush, stream, dev)
     # ---- Ulysses region: both All-to-Alls fused vs the post-only fused call
     # (the difference is the cost of reading from the sequence partition) and
     # vs the serial composition
     if uly_ok:
-        t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps)
+        t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps,
+                                                        flush, stream, dev)
+    # ---- sustained region: the fused call back to back for a few seconds, no
+    # flush between launches (the inputs of the long workloads exceed L2 anyway)
+    sustained = None
+    if args.sustain_seconds > 0:
+        t_one = statistics.median(t_fused) * 1e-3
+        n = max(3, int(math.ceil(args.sustain_seconds / max(t_one, 1e-6))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fused()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        s_ms = e0.elapsed_time(e1)
+        s_tf = n * flops / (s_ms * 1e-3) / 1e12
+        sustained = {"launches": n, "seconds": s_ms * 1e-3, "tflops": s_tf,
+                     "frac_sustained_peak": s_tf / (peaks["bf16_tflops_sustained"] * (4.0 / 3.0 if args.q8 else 1.0)),
+                     "frac_burst_peak": s_tf / (peaks["bf16_tflops"] * (4.0 / 3.0 if args.q8 else 1.0)),
+                     "what": "the timed call launched back to back (no L2 flush), one event pair around all"}
     clocks = sampler.stop()
     assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
+
+    # ---- epilogue store spans (traced fused call on this workload)
+    epilogue = None
+    if D == 128 and S % 128 == 0 and not args.q8 and not args.causal:
+        epilogue = epilogue_spans(xs, q, k, v, out_whole, w, flush, stream, dev, clocks.get("sm_mhz"), peaks["hbm_gbs"])
+    else:
+        epilogue = {"unavailable": "the traced call is built for bf16, non-causal, D = 128, S % 128 == 0"}
 
     # ---- end to end through the C ABI with host buffers
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
@@ -471,18 +617,28 @@ def run_ours(args):
     e2e_max = reduce_max(sum(e2e_ms), world, dev)
     e2e_value = world * flops * args.steps / (e2e_max * 1e-3) / 1e12
 
+    # ---- every synthetic configuration (bf16, non-causal): the section 5.3
+    # comparison at each, for the per-configuration view of the metric
+    main_entry = comparison_entry(w, flops, nbytes, peaks, *t_cmp)
+    per_config = None
+    if not args.no_per_config and rank == 0:
+        per_config = []
+        for idx in range(5):
+            if idx == args.workload and not args.q8 and not args.causal:
+                e = dict(main_entry)
+            else:
+                e = measure_config(idx, args.steps, args.warmup, flush, stream, dev, peaks)
+            e["config_index"] = idx
+            per_config.append(e)
+
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
     med = lambda xs_: statistics.median(xs_)
-    tf_us, ta_us, ts_us, tp_us = (1e3 * med(t) for t in (t_fused, t_attn, t_serial, t_perm))
-    tfc_us, tw_us = 1e3 * med(t_fused_cmp), 1e3 * med(t_whole)
-    e_res = tfc_us - ta_us
-    hiding = 1.0 - e_res / (ts_us - ta_us) if ts_us > ta_us else None
+    tf_us = 1e3 * med(t_fused)
     kernel_tflops = flops / (tf_us * 1e-6) / 1e12
     traffic = recorded_traffic(w["name"] + (" causal" if args.causal else "")
                                + (" e4m3 qkv" if args.v8 else " e4m3" if args.q8 else ""))
@@ -506,6 +662,10 @@ def run_ours(args):
         }
     else:
         uly = {"unavailable": uly_why}
+    tfc_us, ta_us, ts_us, tp_us, tw_us = (main_entry[key] for key in ("t_fused_us", "t_attn_us", "t_serial_us",
+                                                                      "permute", "t_fused_whole_items_us"))
+    tp_us = tp_us["t_us"]
+    e_res = tfc_us - ta_us
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -531,10 +691,9 @@ def run_ours(args):
         "overhead_us_vs_attn_only": e_res,
         "t_fused_us": tf_us, "t_fused_interleaved_us": tfc_us, "t_attn_us": ta_us, "t_serial_us": ts_us,
         "t_permute_us": tp_us, "t_fused_whole_items_us": tw_us,
-        "e_res_us": e_res, "hiding_ratio": hiding, "speedup_vs_serial": ts_us / tfc_us,
+        "e_res_us": e_res, "hiding_ratio": main_entry["hiding_ratio"], "speedup_vs_serial": ts_us / tfc_us,
         "workspace_bytes": ws_bytes,
-        "permute": {"gbs": 2 * nbytes / (tp_us * 1e-6) / 1e9, "frac_hbm": 2 * nbytes / (tp_us * 1e-6) / 1e9 /
-                    peaks["hbm_gbs"], "bytes_per_launch": 2 * nbytes},
+        "permute": main_entry["permute"],
         "roofline": {"bound": "tensor",
                      "kernel": ("attn_fwd_kernel<D, scatter, E4M3 q/k/v> (balanced schedule)" if args.v8
                                 else "attn_fwd_kernel<D, scatter, E4M3 q/k> (balanced schedule)" if args.q8
@@ -545,6 +704,9 @@ def run_ours(args):
                      "peak_source": peak_note, "traffic": traffic,
                      "algorithmic_flop_per_launch": flops,
                      "algorithmic_min_bytes_per_launch": 2 * qk_bytes + v_bytes + nbytes},
+        "epilogue": epilogue,
+        "sustained": sustained,
+        "per_config": per_config,
         "ulysses": uly,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "call": e2e_call, "h2d_bytes_per_step": 2 * qk_bytes + v_bytes,
                 "d2h_bytes_per_step": nbytes,
@@ -552,7 +714,7 @@ def run_ours(args):
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
-    if not args.no_cpu_baseline and world >= 1:
+    if not args.no_cpu_baseline:
         rate, rows, wall, threads = oracle_rows_rate(w, q_h, k_h, v_h, args.cpu_seconds, causal=args.causal,
                                                      q8=args.q8)
         line["cpu_baseline"] = {
@@ -564,15 +726,90 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- sequence-length sweep
+
+def sweep_m(lengths, reps: int = 10, H: int = 24, D: int = 128, P: int = 8, B: int = 1):
+    """FA-only, Serial and Fused over the full sequence length M, in the structure
+    of the X-Stage paper's Table 3 (section 5.3): times, E_res = T_fused - T_FA,
+    the hiding ratio H = 1 - (T_fused - T_FA) / (T_serial - T_FA) (Eq. 21) and the
+    speedup over Serial. B = 1, H = 24, D = 128, P = 8 and N(0, 1) bf16 inputs
+    (the pages state no batch, head or rank count for that table). Balanced
+    schedule with a workspace; L2 flushed before every launch; medians of `reps`
+    interleaved, rotated repetitions."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    import xsgen
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    rows = []
+    for S in lengths:
+        q, k, v = (_torch_dev(a, dev) for a in xsgen.random_inputs(3000 + S // 1024, P, B, S, H, D))
+        out, head, serial = (torch.empty_like(q) for _ in range(3))
+        nb = xs.workspace_size(B, S, H, D, P)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        scale = D ** -0.5
+        fused = lambda: xs.attn_a2a_ws(q, k, v, out, B, S, H, D, P, scale, ws, nb, stream=sptr)
+        attn = lambda: xs.attn_ws(q, k, v, head, B, S, H, D, P, scale, ws, nb, stream=sptr)
+
+        def ser():
+            attn()
+            xs.a2a_permute(head, serial, B, S, H, D, P, stream=sptr)
+
+        fns = [attn, ser, fused]
+        for f in fns:
+            f()
+        torch.cuda.synchronize(dev)
+        t = timed(fns, reps, flush, stream, dev)
+        assert xs.device_status(sptr) == xs.XS_OK, xs.last_error()
+        t_fa, t_ser, t_fu = (1e3 * statistics.median(x) for x in t)
+        flops = 4.0 * B * H * S * S * D
+        e_res = t_fu - t_fa
+        rows.append(dict(M=S, t_fa_us=t_fa, t_serial_us=t_ser, t_fused_us=t_fu, e_res_us=e_res,
+                         hiding=(1.0 - e_res / (t_ser - t_fa)) if t_ser > t_fa else None,
+                         speedup_vs_serial=t_ser / t_fu, fused_tflops=flops / (t_fu * 1e-6) / 1e12))
+        del q, k, v, out, head, serial, ws
+        torch.cuda.empty_cache()
+    return rows
+
+
+def sweep_markdown(rows) -> str:
+    cols = ["M"] + [str(r["M"]) for r in rows]
+    out = ["| " + " | ".join(cols) + " |", "|" + "---|" * len(cols)]
+    fmt = [("FA-only (µs)", "t_fa_us", "{:.1f}"), ("Serial: FA then permute (µs)", "t_serial_us", "{:.1f}"),
+           ("Fused (µs)", "t_fused_us", "{:.1f}"), ("E_res = T_fused − T_FA (µs)", "e_res_us", "{:+.1f}"),
+           ("hiding ratio H", "hiding", "{:.0%}"), ("speedup vs Serial", "speedup_vs_serial", "{:.3f}×"),
+           ("fused TFLOP/s", "fused_tflops", "{:.0f}")]
+    for name, key, f in fmt:
+        out.append("| " + " | ".join([name] + ["—" if r[key] is None else f.format(r[key]) for r in rows]) + " |")
+    return "\n".join(out)
+
+
+def run_sweep(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    rows = sweep_m([int(x) for x in args.lengths.split(",")], args.reps)
+    print(sweep_markdown(rows))
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(rows, f, indent=1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=1, help="index into the five synthetic workloads")
+    ap.add_argument("--workload", type=int, default=4,
+                    help="index into the synthetic workloads (default 4: B=2 S=16384 H=40 D=128 P=4, the largest)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the comparison at every configuration")
+    ap.add_argument("--sustain-seconds", type=float, default=3.0,
+                    help="length of the back-to-back region (0: skip it)")
     ap.add_argument("--causal", action="store_true",
                     help="time causal attention (query i sees keys 0..i) instead of full attention")
     ap.add_argument("--q8", action="store_true",
@@ -581,7 +818,15 @@ def main(argv=None):
                     help="time the call with E4M3 queries, keys and values (D = 128 workloads)")
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="oracle seconds per step for --impl reference (default: sized to the run)")
+    ap.add_argument("--sweep-m", action="store_true",
+                    help="instead of the bench line: FA-only / Serial / Fused over the sequence lengths --lengths")
+    ap.add_argument("--lengths", default="8192,16384,32768,49152,65536")
+    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--json", default=None, help="--sweep-m: also write the rows to this JSON file")
     args = ap.parse_args(argv)
+    if args.sweep_m:
+        run_sweep(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     args.v8 = args.qkv8
