@@ -9,7 +9,8 @@ tile into its rank slice) over one batch of the synthetic workload. The default
 workload is the largest: B=2, S=16384, H=40, D=128, P=4 with Q, K ~ N(0, 2)
 (peaked softmax). The inputs (PCG32 -> Box-Muller -> bf16, seed 1000 + workload
 index) are resident in HBM before timing starts. Each timed launch is preceded
-by a 512 MiB write that flushes the 129 MB L2, and timed by CUDA events
+by a 512 MiB write and a 256 MiB read that flush the 129 MB L2 (the read
+writes back the dirty lines of the write before the launch), and timed by CUDA events
 recorded on the launch stream around that launch alone; W untimed warm-up steps
 come first, and the timed region is bracketed by a barrier and
 torch.cuda.synchronize().
@@ -65,6 +66,24 @@ if ROOT not in sys.path:
 METRIC = "fused attn+A2A-scatter TFLOP/s, % BF16 dense peak, µs overhead vs attn-only"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+L2_EVICT_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Empties the 129 MB L2 before a timed launch: a 512 MiB write, then a
+    256 MiB read of a second buffer. The write alone leaves the L2 full of dirty
+    lines, whose write-back the next kernel would pay for (about 4-7 µs at the
+    bench's sizes, measured); the read evicts them first, so the timed kernel
+    starts from a cold and clean L2 and its inputs are not in it."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.evict = torch.ones(L2_EVICT_BYTES // 8, dtype=torch.int64, device=dev)
+
+    def __call__(self, value: int = 0):
+        self.buf.fill_(value & 0xFF)
+        self.evict.max()
 
 
 # ----------------------------------------------------------------- host helpers
@@ -320,7 +339,7 @@ def timed(fns, steps, flush, stream, dev):
         order = list(range(len(fns)))
         order = order[s % len(order):] + order[:s % len(order)]
         for i in order:
-            flush.fill_(s & 0xFF)
+            flush(s)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fns[i]()
@@ -397,7 +416,7 @@ def epilogue_spans(xs, q, k, v, out, w, flush, stream, dev, sm_mhz, hbm_gbs):
     trace = torch.zeros(tbytes // 8, dtype=torch.int64, device=dev)
     sp = stream.cuda_stream
     xs.attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, trace, tbytes, stream=sp)
-    flush.fill_(7)
+    flush(7)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     xs.attn_a2a_trace(q, k, v, out, B, S, H, D, P, scale, trace, tbytes, stream=sp)
@@ -469,7 +488,7 @@ def run_ours(args):
     out_whole = torch.empty_like(out)
     ws_bytes = xs.workspace_size(B, S, H, D, P)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
@@ -599,7 +618,7 @@ def run_ours(args):
         e2e_call = "cudaMemcpyAsync of q, k, v, then the timed call, then cudaMemcpyAsync of out, on one stream"
     e2e_ms = []
     for s in range(args.warmup + args.steps):
-        flush.fill_(s & 0xFF)
+        flush(s)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         if host_call:
@@ -678,7 +697,8 @@ def run_ours(args):
                        + ("; q, k and v rounded to E4M3" if args.v8 else "; q and k rounded to E4M3" if args.q8
                           else "")),
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write",
+            "l2": (f"flushed before every timed launch by a {L2_FLUSH_BYTES >> 20} MiB write, then a "
+                   f"{L2_EVICT_BYTES >> 20} MiB read that writes the dirty lines back before the launch"),
             "timing": "CUDA events on the launch stream around each launch; value = K * flop / sum of times",
             "call": ("xs_attn_a2a_qkv8 (E4M3 q, k and v, balanced schedule, caller-allocated workspace)" if args.v8
                      else "xs_attn_a2a_q8 (E4M3 q and k, balanced schedule, caller-allocated workspace)" if args.q8
@@ -741,7 +761,7 @@ def sweep_m(lengths, reps: int = 10, H: int = 24, D: int = 128, P: int = 8, B: i
     import xsgen
 
     dev = torch.device("cuda", 0)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     rows = []

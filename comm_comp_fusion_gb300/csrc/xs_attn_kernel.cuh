@@ -334,11 +334,11 @@ __device__ __forceinline__ const float *piece_record(const AttnParams &p, int c,
 // this CTA is read from tensor memory (it never went to the workspace);
 // otherwise every piece, this CTA's included, comes from the workspace. Both
 // read the same bits, so the result does not depend on which piece merges.
-// CH columns (32 or 64) are gathered per round.
-template <int D, int CH, bool RAG>
+// CH columns (16, 32 or 64) are gathered per round.
+template <int D, int CH, bool RAG, typename DstFn>
 __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, int lane, uint32_t stage, int c_first,
                                            int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
-                                           uint32_t tO, int64_t dst, bool valid) {
+                                           uint32_t tO, DstFn dst_fn, bool valid) {
     using R = Rec<D>;
     const int self = (int)blockIdx.x;
     float M = -INFINITY;
@@ -367,12 +367,19 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
         for (int c = c_first; c <= c_last; ++c) {
             if (self_tmem && c == self) {
                 const float wk = ex2_approx(m_self - M);
+                if constexpr (CH == 16) {
+                    uint32_t o[16];
+                    tmem_ld16(tO + col0, o);
 #pragma unroll
-                for (int h = 0; h < CH; h += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + col0 + h, o);
+                    for (int i = 0; i < 16; ++i) acc[i] = fmaf(wk, __uint_as_float(o[i]), acc[i]);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[h + i] = fmaf(wk, __uint_as_float(o[i]), acc[h + i]);
+                    for (int h = 0; h < CH; h += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + col0 + h, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[h + i] = fmaf(wk, __uint_as_float(o[i]), acc[h + i]);
+                    }
                 }
             } else {
                 const float *r = piece_record(p, c, ua, R::kFloats);
@@ -398,9 +405,9 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
                             pack_bf16x2(acc[8 * c + 4] * inv_L, acc[8 * c + 5] * inv_L),
                             pack_bf16x2(acc[8 * c + 6] * inv_L, acc[8 * c + 7] * inv_L));
             if ((col0 + CH) % 64 == 0)
-                flush_block<RAG>(p.out, stage, lane, dst, col0 / 64);
+                flush_block<RAG>(p.out, stage, lane, dst_fn(), col0 / 64);
             else if (col0 + CH == D)  // the half block of D = 96
-                flush_block<RAG, 4>(p.out, stage, lane, dst, col0 / 64);
+                flush_block<RAG, 4>(p.out, stage, lane, dst_fn(), col0 / 64);
         }
     }
 }
@@ -410,10 +417,10 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
 // TMEM) and return 0, or publish this piece's rows (unnormalised O, row max,
 // row sum) to the workspace and return 1: the caller must then count the
 // arrival with arrive_piece. `release` runs once the rows are out of TMEM.
-template <int D, int CH, bool RAG, typename Release>
+template <int D, int CH, bool RAG, typename DstFn, typename Release>
 __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
                                                  uint32_t stage, int c_first, int c_last, uint32_t ua, float m, float l,
-                                                 uint32_t tO, int64_t dst, bool valid, Release release) {
+                                                 uint32_t tO, DstFn dst_fn, bool valid, Release release) {
     using R = Rec<D>;
     const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
     const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
@@ -423,20 +430,25 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
     others = __shfl_sync(0xffffffffu, others, 0);
     if (others) {
         __threadfence();
-        merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst, valid);
+        merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst_fn, valid);
         release();
         return 0;
     }
     const int own_slot = 2 * (int)blockIdx.x + (g.first ? 0 : 1);
     float *rec = p.ws_rec + (size_t)own_slot * R::kFloats;
     float4 *o4 = reinterpret_cast<float4 *>(rec) + (size_t)t * (D / 4) * 128;
+    // CH columns (16 or 32) per round
+    constexpr int W = CH < 32 ? 16 : 32;
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
-        if (c + 32 == D) release();
+    for (int c = 0; c < D; c += W) {
+        uint32_t o[W];
+        if constexpr (W == 16)
+            tmem_ld16(tO + c, o);
+        else
+            tmem_ld32(tO + c, o);
+        if (c + W == D) release();
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < W / 4; ++q)
             o4[(size_t)(c / 4 + q) * 128 + row] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
                                                               __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
     }
@@ -447,9 +459,9 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
 
 // Counts this piece's arrival for tile t (after its rows were published and
 // fenced); the last arrival merges from the workspace.
-template <int D, int CH, bool RAG>
+template <int D, int CH, bool RAG, typename DstFn>
 __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
-                                             uint32_t stage, int c_first, int c_last, uint32_t ua, int64_t dst,
+                                             uint32_t stage, int c_first, int c_last, uint32_t ua, DstFn dst_fn,
                                              bool valid) {
     const uint32_t x_local = (uint32_t)(g.item - p.sk_item0);
     uint32_t last = 0;
@@ -460,7 +472,7 @@ __device__ __forceinline__ void arrive_piece(const AttnParams &p, const Seg &g, 
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
-    merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, false, 0.f, 0.f, 0u, dst, valid);
+    merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, false, 0.f, 0.f, 0u, dst_fn, valid);
 }
 
 
@@ -842,6 +854,9 @@ __global__ void __launch_bounds__(512, 1)
         sched_init(sch, p);
         Seg g;
         for (; ok && sched_next<CAU>(sch, p, g); ++it) {
+            // this CTA's last piece of a split item is finished here (decided now,
+            // while few values are live)
+            const bool finish_here = g.split && sched_done<CAU>(sch, p);
             float m = 0.f, l = 0.f;
             // causal: this tile's diagonal K/V tile (its last step) is 2p + t
             const int qt_diag = CAU ? 2 * (g.item % p.n_pairs) + t : -1;
@@ -976,7 +991,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
             }
             if (!ok) break;
-            if (g.split && sched_done<CAU>(sch, p)) {
+            if (finish_here) {
                 // This CTA's last piece of a split item: finish tile t here, both
                 // tiles in parallel, instead of handing it to the epilogue. Every
                 // MMA of the CTA is complete once O_t is final, so the query
@@ -989,14 +1004,15 @@ __global__ void __launch_bounds__(512, 1)
                 const int c_first = sk_cta_of(ua, p), c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
-                const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row);
+                // the destination row is computed where it is stored
+                auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
                 const uint32_t stage = sQ + t * C::kQKTile + (warp & 3) * C::kStageWarp;
-                const uint32_t pend = finish_piece<D, D % 64 ? 32 : 64, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
-                                                          l, tO, dst, valid, [] {});
+                const uint32_t pend = finish_piece<D, 16, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
+                                                          l, tO, dst_fn, valid, [] {});
                 if (pend) {
                     __threadfence();
                     __syncwarp();
-                    arrive_piece<D, D % 64 ? 32 : 64, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst, valid);
+                    arrive_piece<D, 16, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
                 }
                 continue;
             }
@@ -1049,8 +1065,9 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
                 };
                 if (g.split) {
-                    pending |= finish_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO, dst,
-                                                   valid, release_o)
+                    auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
+                    pending |= finish_piece<D, 16, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
+                                                        dst_fn, valid, release_o)
                                << t;
                     continue;
                 }
@@ -1061,34 +1078,25 @@ __global__ void __launch_bounds__(512, 1)
                     g_ready = globaltimer_ns();
                 }
 #pragma unroll 1
-                for (int db = 0; db < D / 64; ++db) {
-                    uint32_t o[64];
-                    tmem_ld64(tO + db * 64, o);
-                    if (db == C::kNDB - 1) release_o();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    // 32 columns per round into the staged rows; a full 128-byte row
+                    // block (or the half block of D = 96) is then stored
+                    uint32_t o[32];
+                    tmem_ld32(tO + c0, o);
+                    if (c0 + 32 == D) release_o();
                     if (!valid) continue;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        stage_chunk(stage, lane, c, pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
+                    for (int c = 0; c < 4; ++c)
+                        stage_chunk(stage, lane, (c0 % 64) / 8 + c,
+                                    pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
                                     pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
-                    if (TRACE && db == 0) t_store = clock64_now();
-                    flush_block<RAG>(p.out, stage, lane, dst, db);
-                }
-                if (D % 64) {  // the last 32 columns of D = 96
-                    uint32_t o[32];
-                    tmem_ld32(tO + (D / 64) * 64, o);
-                    release_o();
-                    if (valid) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            stage_chunk(stage, lane, c,
-                                        pack_bf16x2(u2f(o[8 * c + 0]) * inv_l, u2f(o[8 * c + 1]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 2]) * inv_l, u2f(o[8 * c + 3]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 4]) * inv_l, u2f(o[8 * c + 5]) * inv_l),
-                                        pack_bf16x2(u2f(o[8 * c + 6]) * inv_l, u2f(o[8 * c + 7]) * inv_l));
-                        flush_block<RAG, 4>(p.out, stage, lane, dst, D / 64);
-                    }
+                    if (TRACE && c0 == 32) t_store = clock64_now();
+                    if ((c0 + 32) % 64 == 0)
+                        flush_block<RAG>(p.out, stage, lane, dst, c0 / 64);
+                    else if (c0 + 32 == D)  // the half block of D = 96
+                        flush_block<RAG, 4>(p.out, stage, lane, dst, c0 / 64);
                 }
                 if (TRACE && lane == 0) {
                     const unsigned long long t_end = clock64_now();
@@ -1108,8 +1116,9 @@ __global__ void __launch_bounds__(512, 1)
             for (int t = 0; t < 2; ++t) {
                 if (!(pending & (1u << t))) continue;
                 const int qt = 2 * w.pair + t;
-                arrive_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
-                                         out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row), qt < p.n_qt);
+                arrive_piece<D, 16, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
+                                         [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); },
+                                         qt < p.n_qt);
             }
         }
     }

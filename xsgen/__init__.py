@@ -92,6 +92,9 @@ WORKLOADS = [
          name="D=96: B=1 S=8192 H=32 D=96 P=8"),
     dict(B=1, S=8192, H=16, D=256, P=8, sigma_qk=1.0, sigma_v=1.0, scale=256 ** -0.5,
          name="D=256: B=1 S=8192 H=16 D=256 P=8"),
+    # head dimension 64 at the flops of the S=8192 workload (H doubled)
+    dict(B=1, S=8192, H=48, D=64, P=8, sigma_qk=1.0, sigma_v=1.0, scale=64 ** -0.5,
+         name="D=64: B=1 S=8192 H=48 D=64 P=8"),
 ]
 
 
