@@ -577,6 +577,20 @@ def run_ours(args):
     if uly_ok:
         t_uly, t_uly_fused, t_uly_serial, t_inv = timed([ulysses, fused, ulysses_serial, inv_perm], args.steps,
                                                         flush, stream, dev)
+    main_entry = comparison_entry(w, flops, nbytes, peaks, *t_cmp)
+    # ---- every synthetic configuration (bf16, non-causal): the section 5.3
+    # comparison at each, for the per-configuration view of the metric
+    per_config = None
+    if not args.no_per_config and rank == 0:
+        per_config = []
+        for idx in range(5):
+            if idx == args.workload and not args.q8 and not args.causal:
+                e = dict(main_entry)
+            else:
+                e = measure_config(idx, args.steps, args.warmup, flush, stream, dev, peaks)
+            e["config_index"] = idx
+            per_config.append(e)
+
     # ---- sustained region: the fused call back to back for a few seconds, no
     # flush between launches (the inputs of the long workloads exceed L2 anyway)
     sustained = None
@@ -635,20 +649,6 @@ def run_ours(args):
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_max = reduce_max(sum(e2e_ms), world, dev)
     e2e_value = world * flops * args.steps / (e2e_max * 1e-3) / 1e12
-
-    # ---- every synthetic configuration (bf16, non-causal): the section 5.3
-    # comparison at each, for the per-configuration view of the metric
-    main_entry = comparison_entry(w, flops, nbytes, peaks, *t_cmp)
-    per_config = None
-    if not args.no_per_config and rank == 0:
-        per_config = []
-        for idx in range(5):
-            if idx == args.workload and not args.q8 and not args.causal:
-                e = dict(main_entry)
-            else:
-                e = measure_config(idx, args.steps, args.warmup, flush, stream, dev, peaks)
-            e["config_index"] = idx
-            per_config.append(e)
 
     if rank != 0:
         if world > 1:

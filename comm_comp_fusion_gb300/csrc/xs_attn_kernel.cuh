@@ -334,7 +334,7 @@ __device__ __forceinline__ const float *piece_record(const AttnParams &p, int c,
 // this CTA is read from tensor memory (it never went to the workspace);
 // otherwise every piece, this CTA's included, comes from the workspace. Both
 // read the same bits, so the result does not depend on which piece merges.
-// CH columns (16, 32 or 64) are gathered per round.
+// CH columns (8, 16, 32 or 64) are gathered per round.
 template <int D, int CH, bool RAG, typename DstFn>
 __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, int lane, uint32_t stage, int c_first,
                                            int c_last, uint32_t ua, bool self_tmem, float m_self, float l_self,
@@ -365,9 +365,10 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
 #pragma unroll
         for (int i = 0; i < CH; ++i) acc[i] = 0.f;
         for (int c = c_first; c <= c_last; ++c) {
-            if (self_tmem && c == self) {
+            if (CH >= 16 && self_tmem && c == self) {  // merges of 8 columns read only the workspace
                 const float wk = ex2_approx(m_self - M);
-                if constexpr (CH == 16) {
+                if constexpr (CH < 16) {
+                } else if constexpr (CH == 16) {
                     uint32_t o[16];
                     tmem_ld16(tO + col0, o);
 #pragma unroll
@@ -413,11 +414,11 @@ __device__ __forceinline__ void merge_rows(const AttnParams &p, int t, int row, 
 }
 
 // One warp's 32 rows of tile t of a split piece, after its last PV: either
-// merge now (every other piece already arrived; this piece is read from
-// TMEM) and return 0, or publish this piece's rows (unnormalised O, row max,
-// row sum) to the workspace and return 1: the caller must then count the
+// merge now (TRY_SELF and every other piece already arrived; this piece is read
+// from TMEM) and return 0, or publish this piece's rows (unnormalised O, row
+// max, row sum) to the workspace and return 1: the caller must then count the
 // arrival with arrive_piece. `release` runs once the rows are out of TMEM.
-template <int D, int CH, bool RAG, typename DstFn, typename Release>
+template <int D, int CH, bool RAG, bool TRY_SELF, typename DstFn, typename Release>
 __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg &g, int t, int wq, int row, int lane,
                                                  uint32_t stage, int c_first, int c_last, uint32_t ua, float m, float l,
                                                  uint32_t tO, DstFn dst_fn, bool valid, Release release) {
@@ -426,9 +427,9 @@ __device__ __forceinline__ uint32_t finish_piece(const AttnParams &p, const Seg 
     const uint32_t npieces = (uint32_t)(c_last - c_first + 1);
     const unsigned long long *cnt = p.ws_cnt + ((size_t)x_local * 8 + t * 4 + wq);
     uint32_t others = 0;
-    if (lane == 0) others = arrivals_now(cnt, p.gen) == npieces - 1u ? 1u : 0u;
+    if (TRY_SELF && lane == 0) others = arrivals_now(cnt, p.gen) == npieces - 1u ? 1u : 0u;
     others = __shfl_sync(0xffffffffu, others, 0);
-    if (others) {
+    if (TRY_SELF && others) {
         __threadfence();
         merge_rows<D, CH, RAG>(p, t, row, lane, stage, c_first, c_last, ua, true, m, l, tO, dst_fn, valid);
         release();
@@ -872,8 +873,7 @@ __global__ void __launch_bounds__(512, 1)
                 uint32_t sa[64], sb[64];
 #define SV(i) u2f((i) < 64 ? sa[(i) & 63] : sb[(i) & 63])
                 if (RAG && !CAU && j == jmask) mask_tail(tS, p.kv_tail);
-                tmem_ld64(tS, sa);
-                tmem_ld64(tS + 64, sb);
+                tmem_ld64x2(tS, sa, sb);
                 if (CAU && j == qt_diag) {
                     // the diagonal tile: keys after this row's token take no weight
                     const uint32_t ninf = f2u(-INFINITY);
@@ -939,8 +939,7 @@ __global__ void __launch_bounds__(512, 1)
                     // Some row sum passed 256: S is still in TMEM (P has not been
                     // stored), so reload it, take the max, move m where it grew by
                     // more than 8 (rescaling O and l) and redo the exponentials.
-                    tmem_ld64(tS, sa);
-                    tmem_ld64(tS + 64, sb);
+                    tmem_ld64x2(tS, sa, sb);
                     if (CAU && j == qt_diag) {
                         const uint32_t ninf = f2u(-INFINITY);
 #pragma unroll
@@ -1007,13 +1006,14 @@ __global__ void __launch_bounds__(512, 1)
                 // the destination row is computed where it is stored
                 auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
                 const uint32_t stage = sQ + t * C::kQKTile + (warp & 3) * C::kStageWarp;
-                const uint32_t pend = finish_piece<D, 16, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m,
-                                                          l, tO, dst_fn, valid, [] {});
-                if (pend) {
-                    __threadfence();
-                    __syncwarp();
-                    arrive_piece<D, 16, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
-                }
+                // publish this piece's rows, then count the arrival; the last one merges
+                // (in rounds of 8 columns: this path runs once per CTA, and the softmax
+                // warps keep their registers for the loop above)
+                (void)finish_piece<D, 16, RAG, false>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m, l, tO,
+                                                      dst_fn, valid, [] {});
+                __threadfence();
+                __syncwarp();
+                arrive_piece<D, 8, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
                 continue;
             }
             ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
@@ -1066,7 +1066,7 @@ __global__ void __launch_bounds__(512, 1)
                 };
                 if (g.split) {
                     auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
-                    pending |= finish_piece<D, 16, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
+                    pending |= finish_piece<D, 16, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
                                                         dst_fn, valid, release_o)
                                << t;
                     continue;
