@@ -1006,14 +1006,16 @@ __global__ void __launch_bounds__(512, 1)
                 // the destination row is computed where it is stored
                 auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
                 const uint32_t stage = sQ + t * C::kQKTile + (warp & 3) * C::kStageWarp;
-                // publish this piece's rows, then count the arrival; the last one merges
-                // (in rounds of 8 columns: this path runs once per CTA, and the softmax
-                // warps keep their registers for the loop above)
-                (void)finish_piece<D, 16, RAG, false>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m, l, tO,
-                                                      dst_fn, valid, [] {});
-                __threadfence();
-                __syncwarp();
-                arrive_piece<D, 8, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
+                // 64 columns per merge round (32 at D = 96): the merges of the balanced
+                // tail end the kernel, so their load latency is on its critical path
+                constexpr int CH = D % 64 ? 32 : 64;
+                const uint32_t pend = finish_piece<D, CH, RAG, true>(p, g, t, warp & 3, row, lane, stage, c_first, c_last,
+                                                                     ua, m, l, tO, dst_fn, valid, [] {});
+                if (pend) {
+                    __threadfence();
+                    __syncwarp();
+                    arrive_piece<D, CH, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
+                }
                 continue;
             }
             ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
@@ -1066,7 +1068,7 @@ __global__ void __launch_bounds__(512, 1)
                 };
                 if (g.split) {
                     auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
-                    pending |= finish_piece<D, 16, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
+                    pending |= finish_piece<D, 32, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
                                                         dst_fn, valid, release_o)
                                << t;
                     continue;
@@ -1116,7 +1118,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int t = 0; t < 2; ++t) {
                 if (!(pending & (1u << t))) continue;
                 const int qt = 2 * w.pair + t;
-                arrive_piece<D, 16, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
+                arrive_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
                                          [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); },
                                          qt < p.n_qt);
             }
