@@ -239,9 +239,9 @@ xs_status pipe_init(HostPipe &hp) {
 
 cudaError_t launch_any(const CallOpts &o, int D, const xs::OperandMaps<1> &maps, const xs::AttnParams &p, int grid,
                        cudaStream_t s) {
-    if (o.causal) return xs::launch_causal(D, o.epi, maps, p, grid, s);
-    if (o.f8) return xs::launch_attention_f8_d128(o.f8, o.epi, maps, p, grid, s);
-    return xs::launch_attention(D, o.epi, maps, p, grid, s);
+    if (o.causal) return xs::launch_causal(D, maps, p, grid, s);
+    if (o.f8) return xs::launch_attention_f8_d128(o.f8, maps, p, grid, s);
+    return xs::launch_attention(D, maps, p, grid, s);
 }
 
 // The host-buffer call: ranks are split into up to kMaxChunks chunks. Chunk c's
@@ -408,6 +408,7 @@ xs_status attention_call(const void *q, const void *k, const void *v, void *out,
     p.n_items = (int)items;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
     p.out = static_cast<uint16_t *>(out);
+    p.head_out = epi ? 0 : 1;
     p.ws_rec = nullptr;
     p.ws_cnt = nullptr;
     p.gen = 0;

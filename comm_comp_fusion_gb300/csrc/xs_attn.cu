@@ -14,12 +14,12 @@ size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms) {
     return rec + cnt;
 }
 
-cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+cudaError_t launch_attention(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                              cudaStream_t stream) {
-    if (D == 256) return launch_attention_d256(epi, maps, p, grid, stream);
-    if (D == 128) return launch_attention_d128(epi, maps, p, grid, stream);
-    if (D == 96) return launch_attention_d96(epi, maps, p, grid, stream);
-    if (D == 64) return launch_attention_d64(epi, maps, p, grid, stream);
+    if (D == 256) return launch_attention_d256(maps, p, grid, stream);
+    if (D == 128) return launch_attention_d128(maps, p, grid, stream);
+    if (D == 96) return launch_attention_d96(maps, p, grid, stream);
+    if (D == 64) return launch_attention_d64(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -29,12 +29,12 @@ cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const Att
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+cudaError_t launch_causal(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                           cudaStream_t stream) {
-    if (D == 256) return launch_causal_d256(epi, maps, p, grid, stream);
-    if (D == 128) return launch_causal_d128(epi, maps, p, grid, stream);
-    if (D == 96) return launch_causal_d96(epi, maps, p, grid, stream);
-    if (D == 64) return launch_causal_d64(epi, maps, p, grid, stream);
+    if (D == 256) return launch_causal_d256(maps, p, grid, stream);
+    if (D == 128) return launch_causal_d128(maps, p, grid, stream);
+    if (D == 96) return launch_causal_d96(maps, p, grid, stream);
+    if (D == 64) return launch_causal_d64(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -233,10 +233,13 @@ __device__ __forceinline__ float4 ld_cg4(const float4 *ptr) {
 }
 
 // Element offset of the first element of output row (rb, hl, token s).
-template <int D, int EPI, bool RAG>
+// p.head_out: head-partitioned like q (attention only); otherwise the row's slot
+// in the sequence partition (the All-to-All scatter). Attention only and the
+// fused call thus run the same compiled kernel.
+template <int D, bool RAG>
 __device__ __forceinline__ int64_t out_row_offset(const AttnParams &p, int rb, int hl, int s) {
     if (RAG && s >= p.S) return -1;  // a row of a partial last tile that does not exist
-    if (EPI == 0) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
+    if (p.head_out) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
     const int b = rb % p.B, r = rb / p.B;
     const int h = r * p.Hl + hl;
     const int rd = s / p.Sl, sl = s - rd * p.Sl;
@@ -491,7 +494,7 @@ __device__ __forceinline__ void seq_position(const AttnParams &p, int s, int &rs
     sl = s - rs * p.Sl;
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU>
+template <int D, int LD, int TRACE, bool RAG, bool CAU>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kSeqMaps : 1> tm, const AttnParams p) {
     using C = Cfg<D>;
@@ -863,7 +866,7 @@ __global__ void __launch_bounds__(512, 1)
                 const Item w = decode_item(p, g.item);
                 const uint32_t ua = (uint32_t)(g.item - p.sk_item0) * (uint32_t)p.n_kv;
                 const int c_first = sk_cta_of(ua, p), c_last = sk_cta_of(ua + (uint32_t)p.n_kv - 1u, p);
-                const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, w.qt * 128 + row);
+                const int64_t dst = out_row_offset<D, RAG>(p, w.rb, w.hl, w.qt * 128 + row);
                 const uint32_t stage = sQ + (warp & 3) * C::kStageWarp;
                 const uint32_t pend = finish_piece<D, D % 64 ? 32 : 64, RAG>(p, g, warp & 3, row, lane, stage,
                                                                              c_first, c_last, ua, m, l, tO, dst,
@@ -918,7 +921,7 @@ __global__ void __launch_bounds__(512, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(BL_EMPTY + ob));
             tc_fence_after();
-            const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, w.qt * 128 + row);
+            const int64_t dst = out_row_offset<D, RAG>(p, w.rb, w.hl, w.qt * 128 + row);
             const uint32_t tO = tmem + lane_base + C::colO(ob);
             auto release_o = [&]() {  // O fully read: a later item may overwrite it
                 tc_fence_before();
@@ -990,10 +993,10 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false>
+template <int D, int LD, int TRACE, bool RAG, bool CAU = false>
 static cudaError_t launch_one(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU>;
+    auto kern = attn_fwd_kernel<D, LD, TRACE, RAG, CAU>;
     // The shared-memory limit is raised once per device and instance: setting a
     // function attribute before every launch makes each launch start much later.
     static std::atomic<uint64_t> configured{0};
@@ -1023,28 +1026,27 @@ static cudaError_t launch_one(const OperandMaps<LD ? kSeqMaps : 1> &maps, const 
 
 // The ragged instances (S not a multiple of 128) carry the key mask and the
 // row guard; the others compile without them.
-template <int D, int EPI, int LD>
+template <int D, int LD>
 static cudaError_t launch_t(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                             cudaStream_t stream) {
-    return p.kv_tail < 128 ? launch_one<D, EPI, LD, 0, true>(maps, p, grid, stream)
-                           : launch_one<D, EPI, LD, 0, false>(maps, p, grid, stream);
+    return p.kv_tail < 128 ? launch_one<D, LD, 0, true>(maps, p, grid, stream)
+                           : launch_one<D, LD, 0, false>(maps, p, grid, stream);
 }
 
 
 // Per-head-dimension entry points; each xs_attn_d<D>.cu instantiates one set.
 #define XS_DEFINE_ATTN1_ENTRY(D)                                                                                   \
-    cudaError_t launch_attention_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
+    cudaError_t launch_attention_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,                   \
                                       cudaStream_t stream) {                                                      \
-        return epi ? launch_t<D, 1, 0>(maps, p, grid, stream) : launch_t<D, 0, 0>(maps, p, grid, stream);          \
+        return launch_t<D, 0>(maps, p, grid, stream);                                                             \
     }                                                                                                             \
     cudaError_t launch_ulysses_d##D(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream) {                                                        \
-        return launch_t<D, 1, 1>(maps, p, grid, stream);                                                          \
+        return launch_t<D, 1>(maps, p, grid, stream);                                                             \
     }                                                                                                             \
-    cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
+    cudaError_t launch_causal_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,                      \
                                    cudaStream_t stream) {                                                         \
-        return epi ? launch_one<D, 1, 0, 0, true, true>(maps, p, grid, stream)                                     \
-                   : launch_one<D, 0, 0, 0, true, true>(maps, p, grid, stream);                                    \
+        return launch_one<D, 0, 0, true, true>(maps, p, grid, stream);                                             \
     }                                                                                                             \
     cudaError_t read_error_word_d##D(unsigned int *value, bool clear) {                                           \
         cudaError_t e = cudaMemcpyFromSymbol(value, g_xs_error, sizeof(unsigned int));                            \

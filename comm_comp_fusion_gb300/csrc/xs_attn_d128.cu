@@ -11,7 +11,7 @@ XS_DEFINE_ATTN_ENTRY(128)
 
 cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                          cudaStream_t stream) {
-    return launch_one<128, 1, 0, 1, false>(maps, p, grid, stream);
+    return launch_one<128, 0, 1, false>(maps, p, grid, stream);
 }
 
 }  // namespace xs

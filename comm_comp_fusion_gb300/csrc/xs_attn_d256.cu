@@ -9,17 +9,15 @@ namespace one {
 XS_DEFINE_ATTN1_ENTRY(256)
 }  // namespace one
 
-cudaError_t launch_attention_d256(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
-                                  cudaStream_t stream) {
-    return one::launch_attention_d256(epi, maps, p, grid, stream);
+cudaError_t launch_attention_d256(const OperandMaps<1> &maps, const AttnParams &p, int grid, cudaStream_t stream) {
+    return one::launch_attention_d256(maps, p, grid, stream);
 }
 cudaError_t launch_ulysses_d256(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,
                                 cudaStream_t stream) {
     return one::launch_ulysses_d256(maps, p, grid, stream);
 }
-cudaError_t launch_causal_d256(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
-                               cudaStream_t stream) {
-    return one::launch_causal_d256(epi, maps, p, grid, stream);
+cudaError_t launch_causal_d256(const OperandMaps<1> &maps, const AttnParams &p, int grid, cudaStream_t stream) {
+    return one::launch_causal_d256(maps, p, grid, stream);
 }
 cudaError_t read_error_word_d256(unsigned int *value, bool clear) { return one::read_error_word_d256(value, clear); }
 

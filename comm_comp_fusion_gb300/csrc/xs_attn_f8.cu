@@ -7,19 +7,15 @@
 namespace xs {
 
 template <int F8>
-static cudaError_t launch_f8(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
-                             cudaStream_t stream) {
-    if (p.kv_tail < 128)
-        return epi ? launch_one<128, 1, 0, 0, true, false, F8>(maps, p, grid, stream)
-                   : launch_one<128, 0, 0, 0, true, false, F8>(maps, p, grid, stream);
-    return epi ? launch_one<128, 1, 0, 0, false, false, F8>(maps, p, grid, stream)
-               : launch_one<128, 0, 0, 0, false, false, F8>(maps, p, grid, stream);
+static cudaError_t launch_f8(const OperandMaps<1> &maps, const AttnParams &p, int grid, cudaStream_t stream) {
+    return p.kv_tail < 128 ? launch_one<128, 0, 0, true, false, F8>(maps, p, grid, stream)
+                           : launch_one<128, 0, 0, false, false, F8>(maps, p, grid, stream);
 }
 
-cudaError_t launch_attention_f8_d128(int f8, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+cudaError_t launch_attention_f8_d128(int f8, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                      cudaStream_t stream) {
-    if (f8 == 1) return launch_f8<1>(epi, maps, p, grid, stream);
-    if (f8 == 2) return launch_f8<2>(epi, maps, p, grid, stream);
+    if (f8 == 1) return launch_f8<1>(maps, p, grid, stream);
+    if (f8 == 2) return launch_f8<2>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

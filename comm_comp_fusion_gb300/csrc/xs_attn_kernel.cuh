@@ -251,10 +251,13 @@ __device__ __forceinline__ float4 ld_cg4(const float4 *ptr) {
 }
 
 // Element offset of the first element of output row (rb, hl, token s).
-template <int D, int EPI, bool RAG>
+// p.head_out: head-partitioned like q (attention only); otherwise the row's slot
+// in the sequence partition (the All-to-All scatter). Attention only and the
+// fused call thus run the same compiled kernel.
+template <int D, bool RAG>
 __device__ __forceinline__ int64_t out_row_offset(const AttnParams &p, int rb, int hl, int s) {
     if (RAG && s >= p.S) return -1;  // a row of a partial last tile that does not exist
-    if (EPI == 0) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
+    if (p.head_out) return (((int64_t)rb * p.S + s) * p.Hl + hl) * D;
     const int b = rb % p.B, r = rb / p.B;
     const int h = r * p.Hl + hl;
     const int rd = s / p.Sl, sl = s - rd * p.Sl;
@@ -530,7 +533,7 @@ static __device__ __noinline__ void mask_tail(uint32_t tS, int kv_tail) {
     tmem_st_wait();
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU, int F8 = 0>
+template <int D, int LD, int TRACE, bool RAG, bool CAU, int F8 = 0>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ OperandMaps<LD ? kSeqMaps : 1> tm, const AttnParams p) {
     using C = Cfg<D, F8>;
@@ -1004,7 +1007,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
                 // the destination row is computed where it is stored
-                auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
+                auto dst_fn = [&]() { return out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row); };
                 const uint32_t stage = sQ + t * C::kQKTile + (warp & 3) * C::kStageWarp;
                 // 64 columns per merge round (32 at D = 96): the merges of the balanced
                 // tail end the kernel, so their load latency is on its critical path
@@ -1059,7 +1062,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const int qt = 2 * w.pair + t;
                 const bool valid = qt < p.n_qt;
-                const int64_t dst = out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row);
+                const int64_t dst = out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row);
                 const uint32_t tO = tmem + lane_base + C::colO(t);
                 auto release_o = [&]() {  // O_t fully read: the next item may overwrite it
                     tc_fence_before();
@@ -1067,7 +1070,7 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0) mbar_arrive(BAR(BO_FREE + t));
                 };
                 if (g.split) {
-                    auto dst_fn = [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); };
+                    auto dst_fn = [&]() { return out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row); };
                     pending |= finish_piece<D, 32, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
                                                         dst_fn, valid, release_o)
                                << t;
@@ -1119,7 +1122,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (!(pending & (1u << t))) continue;
                 const int qt = 2 * w.pair + t;
                 arrive_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
-                                         [&]() { return out_row_offset<D, EPI, RAG>(p, w.rb, w.hl, qt * 128 + row); },
+                                         [&]() { return out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row); },
                                          qt < p.n_qt);
             }
         }
@@ -1136,10 +1139,10 @@ __global__ void __launch_bounds__(512, 1)
 #undef BAR
 }
 
-template <int D, int EPI, int LD, int TRACE, bool RAG, bool CAU = false, int F8 = 0>
+template <int D, int LD, int TRACE, bool RAG, bool CAU = false, int F8 = 0>
 static cudaError_t launch_one(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                               cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, EPI, LD, TRACE, RAG, CAU, F8>;
+    auto kern = attn_fwd_kernel<D, LD, TRACE, RAG, CAU, F8>;
     using CQ = Cfg<D, F8>;
     // The shared-memory limit is raised once per device and instance: setting a
     // function attribute before every launch makes each launch start much later.
@@ -1170,28 +1173,27 @@ static cudaError_t launch_one(const OperandMaps<LD ? kSeqMaps : 1> &maps, const 
 
 // The ragged instances (S not a multiple of 128) carry the key mask and the
 // row guard; the others compile without them.
-template <int D, int EPI, int LD>
+template <int D, int LD>
 static cudaError_t launch_t(const OperandMaps<LD ? kSeqMaps : 1> &maps, const AttnParams &p, int grid,
                             cudaStream_t stream) {
-    return p.kv_tail < 128 ? launch_one<D, EPI, LD, 0, true>(maps, p, grid, stream)
-                           : launch_one<D, EPI, LD, 0, false>(maps, p, grid, stream);
+    return p.kv_tail < 128 ? launch_one<D, LD, 0, true>(maps, p, grid, stream)
+                           : launch_one<D, LD, 0, false>(maps, p, grid, stream);
 }
 
 
 // Per-head-dimension entry points; each xs_attn_d<D>.cu instantiates one set.
 #define XS_DEFINE_ATTN_ENTRY(D)                                                                                   \
-    cudaError_t launch_attention_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
+    cudaError_t launch_attention_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,                   \
                                       cudaStream_t stream) {                                                      \
-        return epi ? launch_t<D, 1, 0>(maps, p, grid, stream) : launch_t<D, 0, 0>(maps, p, grid, stream);          \
+        return launch_t<D, 0>(maps, p, grid, stream);                                                             \
     }                                                                                                             \
     cudaError_t launch_ulysses_d##D(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream) {                                                        \
-        return launch_t<D, 1, 1>(maps, p, grid, stream);                                                          \
+        return launch_t<D, 1>(maps, p, grid, stream);                                                             \
     }                                                                                                             \
-    cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
+    cudaError_t launch_causal_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,                      \
                                    cudaStream_t stream) {                                                         \
-        return epi ? launch_one<D, 1, 0, 0, true, true>(maps, p, grid, stream)                                     \
-                   : launch_one<D, 0, 0, 0, true, true>(maps, p, grid, stream);                                    \
+        return launch_one<D, 0, 0, true, true>(maps, p, grid, stream);                                             \
     }                                                                                                             \
     cudaError_t read_error_word_d##D(unsigned int *value, bool clear) {                                           \
         cudaError_t e = cudaMemcpyFromSymbol(value, g_xs_error, sizeof(unsigned int));                            \

@@ -30,6 +30,7 @@ struct AttnParams {
     int item0 = 0;  // global index of work item 0 (a call over the ranks from rank0 on: rank0 * B * Hl * items per head)
     float scale_log2;  // scale * log2(e): softmax runs in base 2
     uint16_t *out;
+    int head_out;          // 1: output head-partitioned like q (attention only); 0: the All-to-All scatter
     int n_dp;              // round-robin waves of whole items
     int sk_item0;          // first item of the balanced region
     uint32_t sk_units;     // units U in the balanced region (0: none), below 2^31
@@ -79,14 +80,15 @@ template <int NM> struct OperandMaps {
     CUtensorMap q[NM], k[NM], v[NM];
 };
 
-// epi = 0: head-partitioned output (same layout as q); epi = 1: All-to-All scatter.
-cudaError_t launch_attention(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+// The output layout is p.head_out (head-partitioned) or the All-to-All scatter;
+// both run the same compiled kernel.
+cudaError_t launch_attention(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                              cudaStream_t stream);
 // The fused call with epilogue tracing (p.trace set, whole-item schedule).
 cudaError_t launch_attention_traced(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                     cudaStream_t stream);
 // Causal attention (query token i sees keys 0..i), whole-item schedule.
-cudaError_t launch_causal(int D, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+cudaError_t launch_causal(int D, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                           cudaStream_t stream);
 // Sequence-partitioned inputs (the pre-attention All-to-All done by the loads),
 // sequence-partitioned output.
@@ -95,11 +97,11 @@ cudaError_t launch_ulysses(int D, const OperandMaps<kSeqMaps> &maps, const AttnP
 
 // Per-head-dimension instances (xs_attn_d64.cu, xs_attn_d96.cu, xs_attn_d128.cu).
 #define XS_DECLARE_ATTN_ENTRY(D)                                                                                  \
-    cudaError_t launch_attention_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
+    cudaError_t launch_attention_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,          \
                                       cudaStream_t stream);                                                       \
     cudaError_t launch_ulysses_d##D(const OperandMaps<kSeqMaps> &maps, const AttnParams &p, int grid,             \
                                     cudaStream_t stream);                                                         \
-    cudaError_t launch_causal_d##D(int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
+    cudaError_t launch_causal_d##D(const OperandMaps<1> &maps, const AttnParams &p, int grid,             \
                                    cudaStream_t stream);                                                          \
     cudaError_t read_error_word_d##D(unsigned int *value, bool clear);
 XS_DECLARE_ATTN_ENTRY(64)
@@ -110,7 +112,7 @@ cudaError_t launch_attention_traced_d128(const OperandMaps<1> &maps, const AttnP
                                          cudaStream_t stream);
 // E4M3 inputs, D = 128 only (xs_attn_f8.cu): f8 = 1 for E4M3 q and k (maps over
 // bytes) with bf16 v, f8 = 2 for E4M3 q, k and v.
-cudaError_t launch_attention_f8_d128(int f8, int epi, const OperandMaps<1> &maps, const AttnParams &p, int grid,
+cudaError_t launch_attention_f8_d128(int f8, const OperandMaps<1> &maps, const AttnParams &p, int grid,
                                      cudaStream_t stream);
 cudaError_t read_error_word_f8(unsigned int *value, bool clear);
 
