@@ -244,14 +244,15 @@ cudaError_t launch_any(const CallOpts &o, int D, const xs::OperandMaps<1> &maps,
     return xs::launch_attention(D, maps, p, grid, s);
 }
 
-// The host-buffer call: ranks are split into up to kMaxChunks chunks. Chunk c's
-// q, k, v slices (contiguous in the head-partitioned layout) are copied in on
+// The host-buffer call: the (rank, batch) slices are split into up to kMaxChunks
+// chunks. Chunk c's q, k, v slices (contiguous in the head-partitioned layout) are copied in on
 // the pipeline's h2d stream; the caller's stream waits for them and runs the
 // attention kernel over that chunk's work items only; the d2h stream then
-// copies the chunk's output out: the columns of its heads in every row of the
-// sequence-partitioned output (one 2-D copy), or its contiguous slice of the
-// head-partitioned one. Copies of later chunks overlap the compute of earlier
-// ones. The caller's stream finally waits for the last copy out.
+// copies the chunk's output out: the columns of its heads in the rows of its
+// batches of the sequence-partitioned output (one 2-D copy when the chunk holds
+// whole ranks, one per slice and destination rank otherwise), or its contiguous
+// part of the head-partitioned one. Copies of later chunks overlap the compute
+// of earlier ones. The caller's stream finally waits for the last copy out.
 xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const void *v, void *out, size_t qk_bytes,
                         size_t v_bytes, size_t bytes, int D, xs::AttnParams p, const xs::OperandMaps<1> &maps,
                         const DeviceInfo &info, int dev, cudaStream_t s) {
@@ -259,9 +260,11 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
     std::lock_guard<std::mutex> lk(hp.mu);
     xs_status st = pipe_init(hp);
     if (st) return st;
-    const int P = p.P, per_rank = p.n_items / P;
-    const int chunks = xs::host_chunks(P, (long long)(2 * qk_bytes + v_bytes), kMaxChunks);
-    const size_t q_rank = qk_bytes / P, v_rank = v_bytes / P, o_rank = bytes / P;
+    // chunks over the P * B (rank, batch) slices: each is contiguous in q, k, v and
+    // owns a contiguous range of work items (items are ordered slice by slice)
+    const int P = p.P, n_rb = P * p.B, per_rb = p.n_items / n_rb;
+    const int chunks = xs::host_chunks(n_rb, (long long)(2 * qk_bytes + v_bytes), kMaxChunks);
+    const size_t q_rb = qk_bytes / n_rb, v_rb = v_bytes / n_rb, o_rb = bytes / n_rb;
     const size_t head_row = (size_t)D * 2, pitch = (size_t)p.H * head_row;
     const char *hq = static_cast<const char *>(o.hq), *hk = static_cast<const char *>(o.hk);
     const char *hv = static_cast<const char *>(o.hv);
@@ -273,33 +276,42 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.start, 0);
     for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
-        const int r0 = (int)((long long)c * P / chunks), r1 = (int)((long long)(c + 1) * P / chunks);
-        const int nr = r1 - r0;
-        e = cudaMemcpyAsync((void *)(dq + r0 * q_rank), hq + r0 * q_rank, nr * q_rank, cudaMemcpyHostToDevice, hp.h2d);
+        const int s0 = (int)((long long)c * n_rb / chunks), s1 = (int)((long long)(c + 1) * n_rb / chunks);
+        const int ns = s1 - s0;
+        e = cudaMemcpyAsync((void *)(dq + s0 * q_rb), hq + s0 * q_rb, ns * q_rb, cudaMemcpyHostToDevice, hp.h2d);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync((void *)(dk + r0 * q_rank), hk + r0 * q_rank, nr * q_rank, cudaMemcpyHostToDevice,
-                                hp.h2d);
+            e = cudaMemcpyAsync((void *)(dk + s0 * q_rb), hk + s0 * q_rb, ns * q_rb, cudaMemcpyHostToDevice, hp.h2d);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync((void *)(dv + r0 * v_rank), hv + r0 * v_rank, nr * v_rank, cudaMemcpyHostToDevice,
-                                hp.h2d);
+            e = cudaMemcpyAsync((void *)(dv + s0 * v_rb), hv + s0 * v_rb, ns * v_rb, cudaMemcpyHostToDevice, hp.h2d);
         if (e == cudaSuccess) e = cudaEventRecord(hp.in[c], hp.h2d);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in[c], 0);
         if (e != cudaSuccess) break;
         xs::AttnParams pc = p;
-        pc.item0 = r0 * per_rank;
-        pc.n_items = nr * per_rank;
+        pc.item0 = s0 * per_rb;
+        pc.n_items = ns * per_rb;
         if (pc.ws_rec) pc.gen = next_generation();
         const int grid = xs::attn_schedule(pc, info.num_sms, pc.ws_rec != nullptr && !o.causal);
         e = launch_any(o, D, maps, pc, grid, s);
         if (e == cudaSuccess) e = cudaEventRecord(hp.comp[c], s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.comp[c], 0);
         if (e != cudaSuccess) break;
-        if (o.epi) {
-            const size_t col = (size_t)r0 * p.Hl * head_row;
-            e = cudaMemcpy2DAsync(hout + col, pitch, dout + col, pitch, (size_t)nr * p.Hl * head_row,
+        if (!o.epi) {
+            e = cudaMemcpyAsync(hout + s0 * o_rb, dout + s0 * o_rb, ns * o_rb, cudaMemcpyDeviceToHost, hp.d2h);
+        } else if (s0 % p.B == 0 && s1 % p.B == 0) {
+            // whole ranks: the columns of their heads in every row of the output
+            const size_t col = (size_t)(s0 / p.B) * p.Hl * head_row;
+            e = cudaMemcpy2DAsync(hout + col, pitch, dout + col, pitch, (size_t)(ns / p.B) * p.Hl * head_row,
                                   (size_t)P * p.B * p.Sl, cudaMemcpyDeviceToHost, hp.d2h);
         } else {
-            e = cudaMemcpyAsync(hout + r0 * o_rank, dout + r0 * o_rank, nr * o_rank, cudaMemcpyDeviceToHost, hp.d2h);
+            // slice (r, b): rank r's head columns in the Sl rows of batch b of each destination rank
+            for (int sb = s0; sb < s1 && e == cudaSuccess; ++sb) {
+                const int r = sb / p.B, b = sb % p.B;
+                for (int rd = 0; rd < P && e == cudaSuccess; ++rd) {
+                    const size_t off = ((size_t)(rd * p.B + b) * p.Sl) * pitch + (size_t)r * p.Hl * head_row;
+                    e = cudaMemcpy2DAsync(hout + off, pitch, dout + off, pitch, (size_t)p.Hl * head_row, (size_t)p.Sl,
+                                          cudaMemcpyDeviceToHost, hp.d2h);
+                }
+            }
         }
     }
     if (e == cudaSuccess) e = cudaEventRecord(hp.done, hp.d2h);

@@ -43,13 +43,14 @@ int attn_schedule(AttnParams &p, int num_sms, bool balanced) {
     return G;
 }
 
-// Chunks of the host-buffer pipeline: one per rank, at most max_chunks, and
-// about 8 MiB of inputs per chunk at least (a chunk's launch costs several
-// microseconds, more than copying a small chunk takes). Chunk c covers ranks
-// [c P / chunks, (c + 1) P / chunks).
-int host_chunks(int P, long long input_bytes, int max_chunks) {
+// Chunks of the host-buffer pipeline over the call's P * B (rank, batch)
+// slices, each contiguous in the head-partitioned inputs: one per slice, at
+// most max_chunks, and about 8 MiB of inputs per chunk at least (a chunk's
+// launch costs several microseconds, more than copying a small chunk takes).
+// Chunk c covers slices [c n / chunks, (c + 1) n / chunks) of the n = slices.
+int host_chunks(int slices, long long input_bytes, int max_chunks) {
     const long long by_size = input_bytes >> 23;
-    int chunks = P < max_chunks ? P : max_chunks;
+    int chunks = slices < max_chunks ? slices : max_chunks;
     if (by_size < chunks) chunks = by_size > 1 ? (int)by_size : 1;
     return chunks;
 }

@@ -1,5 +1,5 @@
 """The host-buffer calls (xs_attn_a2a_host, xs_attn_host): copies in, compute and
-copies out pipelined over rank chunks. Results must equal the device-buffer
+copies out pipelined over chunks of (rank, batch) slices. Results must equal the device-buffer
 calls: bit for bit on the whole-item schedule, and within the parity bar (and
 against the oracle) on the balanced one, whose chunks split items differently."""
 import numpy as np
@@ -17,11 +17,14 @@ CASES = [
     (1, 1000, 4, 128, 2),    # ragged S
     (1, 512, 4, 256, 2),     # D = 256 (single-tile kernel)
 ]
-# large enough for several chunks (about 8 MiB of inputs each, at most one per rank, at most 16)
+# large enough for several chunks (about 8 MiB of inputs each, at most one per (rank,
+# batch) slice, at most 16)
 MULTI = [
     (1, 4096, 24, 128, 8),   # the DiT shape: 8 chunks, one rank each
     (1, 8192, 32, 128, 32),  # 16 chunks of two ranks each
     (1, 4032, 24, 128, 8),   # ragged S, 8 chunks
+    (2, 8192, 8, 128, 2),    # B = 2: 4 chunks of one (rank, batch) slice, so ranks are split
+    (3, 4096, 12, 64, 4),    # B = 3: 12 slices in 6 chunks of 2 (inputs 57 MB), chunks straddle ranks
 ]
 
 

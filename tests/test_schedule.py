@@ -27,7 +27,7 @@ int main() {
         xs::AttnParams p{};
         p.n_items = (int)items;
         p.n_kv = (int)nkv;
-        if (bal == 2) {  // host pipeline chunks: items = P, nkv = input bytes, sms = the cap
+        if (bal == 2) {  // host pipeline chunks: items = (rank, batch) slices, nkv = input bytes, sms = the cap
             std::printf("%d\n", xs::host_chunks((int)items, nkv, sms));
             continue;
         }
@@ -118,10 +118,10 @@ def test_grid_rule_examples(schedule):
 
 
 def test_host_pipeline_chunks(schedule):
-    """One chunk per rank, at most 16, and at least about 8 MiB of inputs per
-    chunk: DiT (P = 8, 75.5 MB of q, k, v) takes 8 chunks, a small call one,
-    P = 32 at S = 8192 the cap of 16. Chunk c's ranks [cP/n, (c+1)P/n) cover
-    every rank once with at least one rank each."""
+    """One chunk per (rank, batch) slice, at most 16, and at least about 8 MiB of
+    inputs per chunk: DiT (8 slices, 75.5 MB of q, k, v) takes 8 chunks, a small
+    call one, 32 slices at S = 8192 the cap of 16. Chunk c's slices
+    [cn/k, (c+1)n/k) cover every slice once with at least one slice each."""
     MB = 1 << 20
     cases = [(8, 75497472, 16, 2), (4, 1 << 20, 16, 2), (32, 3 * 32 * 8192 * 128 * 2 * 4, 16, 2),
              (8, 20 * MB, 16, 2), (1, 10 ** 9, 16, 2), (3, 0, 16, 2)]
