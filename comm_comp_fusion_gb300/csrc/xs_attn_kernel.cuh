@@ -857,11 +857,14 @@ __global__ void __launch_bounds__(512, 1)
         Sched sch;
         sched_init(sch, p);
         Seg g;
+        float m = 0.f, l = 0.f;
+        bool finish = false;
         for (; ok && sched_next<CAU>(sch, p, g); ++it) {
-            // this CTA's last piece of a split item is finished here (decided now,
-            // while few values are live)
-            const bool finish_here = g.split && sched_done<CAU>(sch, p);
-            float m = 0.f, l = 0.f;
+            // this CTA's last piece of a split item is finished by the softmax
+            // warpgroups, after this loop (decided now, while few values are live)
+            finish = g.split && sched_done<CAU>(sch, p);
+            m = 0.f;
+            l = 0.f;
             // causal: this tile's diagonal K/V tile (its last step) is 2p + t
             const int qt_diag = CAU ? 2 * (g.item % p.n_pairs) + t : -1;
             const int nseg = CAU ? min(qt_diag + 1, g.j1 - g.j0) : g.j1 - g.j0;
@@ -992,14 +995,23 @@ __global__ void __launch_bounds__(512, 1)
                 if (TRACE && (warp & 3) == 0 && lane == 0) STEP_TIME(it, t, j, 1, clock64_now());
                 if (lane == 0) mbar_arrive(BAR(BP_FULL + t));
             }
+            if (!ok || finish) break;
+            ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
             if (!ok) break;
-            if (finish_here) {
-                // This CTA's last piece of a split item: finish tile t here, both
-                // tiles in parallel, instead of handing it to the epilogue. Every
-                // MMA of the CTA is complete once O_t is final, so the query
-                // tile's shared memory is free and serves as staging.
-                ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteSoftO);
-                if (!ok) break;
+            row_ml[t * 256 + row] = l;
+            row_ml[t * 256 + 128 + row] = m;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(BL_FULL + t));
+        }
+        if (ok && finish) {
+            // This CTA's last piece of a split item: tile t is finished here, both
+            // tiles in parallel, instead of by the epilogue. It is done after the
+            // item loop, where the loop's values are dead; inside the loop, next
+            // to the softmax's registers, ptxas spilled. Every MMA that reads Q_t
+            // is complete once O_t is final, so the query tile's shared memory is
+            // free and serves as staging.
+            ok = warp_bwait(BAR(BO_FINAL + t), it & 1u, abort_flag, kSiteSoftO);
+            if (ok) {
                 tc_fence_after();
                 const Item w = decode_item(p, g.item);
                 const uint32_t ua = (uint32_t)(g.item - p.sk_item0) * (uint32_t)p.n_kv;
@@ -1012,25 +1024,23 @@ __global__ void __launch_bounds__(512, 1)
                 // 64 columns per merge round (32 at D = 96): the merges of the balanced
                 // tail end the kernel, so their load latency is on its critical path
                 constexpr int CH = D % 64 ? 32 : 64;
-                const uint32_t pend = finish_piece<D, CH, RAG, true>(p, g, t, warp & 3, row, lane, stage, c_first, c_last,
-                                                                     ua, m, l, tO, dst_fn, valid, [] {});
-                if (pend) {
-                    __threadfence();
-                    __syncwarp();
-                    arrive_piece<D, CH, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
-                }
-                continue;
+                // The piece always goes to the workspace and the last of the item's
+                // pieces to arrive merges them all from there. Merging at once from
+                // tensor memory when the others are in saves about 3 us at DiT size,
+                // but next to the softmax's registers ptxas then spilled.
+                finish_piece<D, CH, RAG, false>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, m, l, tO,
+                                                dst_fn, valid, [] {});
+                __threadfence();
+                __syncwarp();
+                arrive_piece<D, CH, RAG>(p, g, t, warp & 3, row, lane, stage, c_first, c_last, ua, dst_fn, valid);
             }
-            ok = warp_bwait(BAR(BL_EMPTY + t), (it & 1u) ^ 1u, abort_flag, kSiteSoftL);
-            if (!ok) break;
-            row_ml[t * 256 + row] = l;
-            row_ml[t * 256 + 128 + row] = m;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(BL_FULL + t));
         }
     } else {
         // ------------------------------------------------------------ epilogue
         setmaxnreg_dec<112>();
+        // columns per merge round of a split item's pieces (16 at D = 96, where 32
+        // made the epilogue spill at 112 registers)
+        constexpr int kEpiMergeCols = D == 96 ? 16 : 32;
         const int wq = warp & 3;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const int row = wq * 32 + lane;
@@ -1071,8 +1081,8 @@ __global__ void __launch_bounds__(512, 1)
                 };
                 if (g.split) {
                     auto dst_fn = [&]() { return out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row); };
-                    pending |= finish_piece<D, 32, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last, ua, m, l, tO,
-                                                        dst_fn, valid, release_o)
+                    pending |= finish_piece<D, kEpiMergeCols, RAG, true>(p, g, t, wq, row, lane, stage, c_first, c_last,
+                                                                        ua, m, l, tO, dst_fn, valid, release_o)
                                << t;
                     continue;
                 }
@@ -1121,7 +1131,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int t = 0; t < 2; ++t) {
                 if (!(pending & (1u << t))) continue;
                 const int qt = 2 * w.pair + t;
-                arrive_piece<D, 32, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
+                arrive_piece<D, kEpiMergeCols, RAG>(p, g, t, wq, row, lane, stage, c_first, c_last, ua,
                                          [&]() { return out_row_offset<D, RAG>(p, w.rb, w.hl, qt * 128 + row); },
                                          qt < p.n_qt);
             }
