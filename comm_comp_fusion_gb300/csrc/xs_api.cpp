@@ -260,10 +260,14 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
     std::lock_guard<std::mutex> lk(hp.mu);
     xs_status st = pipe_init(hp);
     if (st) return st;
-    // chunks over the P * B (rank, batch) slices: each is contiguous in q, k, v and
-    // owns a contiguous range of work items (items are ordered slice by slice)
-    const int P = p.P, n_rb = P * p.B, per_rb = p.n_items / n_rb;
-    const int chunks = xs::host_chunks(n_rb, (long long)(2 * qk_bytes + v_bytes), kMaxChunks);
+    // Chunks over the call's units, one head of one (rank, batch) slice each, in
+    // work-item order: a chunk's items are one contiguous range, and its rows are
+    // whole slices (contiguous) and at most two partial slices (the same heads of
+    // every row: one strided copy each).
+    const int P = p.P, n_rb = P * p.B, Hl = p.Hl, units = n_rb * Hl, per_unit = p.n_items / units;
+    int bounds[kMaxChunks + 1];
+    const int chunks = xs::host_chunk_plan(units, (long long)((2 * qk_bytes + v_bytes) / units), 8ll << 20,
+                                           kMaxChunks, bounds);
     const size_t q_rb = qk_bytes / n_rb, v_rb = v_bytes / n_rb, o_rb = bytes / n_rb;
     const size_t head_row = (size_t)D * 2, pitch = (size_t)p.H * head_row;
     const char *hq = static_cast<const char *>(o.hq), *hk = static_cast<const char *>(o.hk);
@@ -272,23 +276,42 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
     const char *dq = static_cast<const char *>(q), *dk = static_cast<const char *>(k);
     const char *dv = static_cast<const char *>(v);
     char *dout = static_cast<char *>(out);
+    // units [u0, u1) of a head-partitioned tensor ([P*B][S][Hl][*], `slice` bytes
+    // per slice) from src to dst
+    auto copy_units = [&](char *dst, const char *src, size_t slice, int u0, int u1, cudaMemcpyKind kind,
+                          cudaStream_t st) -> cudaError_t {
+        const size_t row = slice / (size_t)p.S, head = row / (size_t)Hl;
+        cudaError_t err = cudaSuccess;
+        for (int u = u0; u < u1 && err == cudaSuccess;) {
+            const int sb = u / Hl, ha = u % Hl;
+            if (ha == 0 && u + Hl <= u1) {  // whole slices [sb, sb1)
+                int sb1 = sb + 1;
+                while ((sb1 + 1) * Hl <= u1) ++sb1;
+                err = cudaMemcpyAsync(dst + sb * slice, src + sb * slice, (size_t)(sb1 - sb) * slice, kind, st);
+                u = sb1 * Hl;
+            } else {  // heads [ha, hb) of every row of slice sb
+                const int hb = ha + (u1 - u < Hl - ha ? u1 - u : Hl - ha);
+                const size_t off = sb * slice + (size_t)ha * head;
+                err = cudaMemcpy2DAsync(dst + off, row, src + off, row, (size_t)(hb - ha) * head, (size_t)p.S, kind, st);
+                u += hb - ha;
+            }
+        }
+        return err;
+    };
     cudaError_t e = cudaEventRecord(hp.start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.start, 0);
     for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
-        const int s0 = (int)((long long)c * n_rb / chunks), s1 = (int)((long long)(c + 1) * n_rb / chunks);
-        const int ns = s1 - s0;
-        e = cudaMemcpyAsync((void *)(dq + s0 * q_rb), hq + s0 * q_rb, ns * q_rb, cudaMemcpyHostToDevice, hp.h2d);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync((void *)(dk + s0 * q_rb), hk + s0 * q_rb, ns * q_rb, cudaMemcpyHostToDevice, hp.h2d);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync((void *)(dv + s0 * v_rb), hv + s0 * v_rb, ns * v_rb, cudaMemcpyHostToDevice, hp.h2d);
+        const int u0 = bounds[c], u1 = bounds[c + 1];
+        e = copy_units((char *)dq, hq, q_rb, u0, u1, cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess) e = copy_units((char *)dk, hk, q_rb, u0, u1, cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess) e = copy_units((char *)dv, hv, v_rb, u0, u1, cudaMemcpyHostToDevice, hp.h2d);
         if (e == cudaSuccess) e = cudaEventRecord(hp.in[c], hp.h2d);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in[c], 0);
         if (e != cudaSuccess) break;
         xs::AttnParams pc = p;
-        pc.item0 = s0 * per_rb;
-        pc.n_items = ns * per_rb;
+        pc.item0 = u0 * per_unit;
+        pc.n_items = (u1 - u0) * per_unit;
         if (pc.ws_rec) pc.gen = next_generation();
         const int grid = xs::attn_schedule(pc, info.num_sms, pc.ws_rec != nullptr && !o.causal);
         e = launch_any(o, D, maps, pc, grid, s);
@@ -296,21 +319,24 @@ xs_status host_pipeline(const CallOpts &o, const void *q, const void *k, const v
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.comp[c], 0);
         if (e != cudaSuccess) break;
         if (!o.epi) {
-            e = cudaMemcpyAsync(hout + s0 * o_rb, dout + s0 * o_rb, ns * o_rb, cudaMemcpyDeviceToHost, hp.d2h);
-        } else if (s0 % p.B == 0 && s1 % p.B == 0) {
+            e = copy_units(hout, dout, o_rb, u0, u1, cudaMemcpyDeviceToHost, hp.d2h);
+        } else if (u0 % (p.B * Hl) == 0 && u1 % (p.B * Hl) == 0) {
             // whole ranks: the columns of their heads in every row of the output
-            const size_t col = (size_t)(s0 / p.B) * p.Hl * head_row;
-            e = cudaMemcpy2DAsync(hout + col, pitch, dout + col, pitch, (size_t)(ns / p.B) * p.Hl * head_row,
+            const size_t col = (size_t)(u0 / Hl / p.B) * Hl * head_row;
+            e = cudaMemcpy2DAsync(hout + col, pitch, dout + col, pitch, (size_t)((u1 - u0) / Hl / p.B) * Hl * head_row,
                                   (size_t)P * p.B * p.Sl, cudaMemcpyDeviceToHost, hp.d2h);
         } else {
-            // slice (r, b): rank r's head columns in the Sl rows of batch b of each destination rank
-            for (int sb = s0; sb < s1 && e == cudaSuccess; ++sb) {
+            // heads [ha, hb) of slice (r, b): rank r's columns of those heads in the Sl
+            // rows of batch b of each destination rank
+            for (int u = u0; u < u1 && e == cudaSuccess;) {
+                const int sb = u / Hl, ha = u % Hl, hb = ha + (u1 - u < Hl - ha ? u1 - u : Hl - ha);
                 const int r = sb / p.B, b = sb % p.B;
                 for (int rd = 0; rd < P && e == cudaSuccess; ++rd) {
-                    const size_t off = ((size_t)(rd * p.B + b) * p.Sl) * pitch + (size_t)r * p.Hl * head_row;
-                    e = cudaMemcpy2DAsync(hout + off, pitch, dout + off, pitch, (size_t)p.Hl * head_row, (size_t)p.Sl,
-                                          cudaMemcpyDeviceToHost, hp.d2h);
+                    const size_t off = ((size_t)(rd * p.B + b) * p.Sl) * pitch + ((size_t)r * Hl + ha) * head_row;
+                    e = cudaMemcpy2DAsync(hout + off, pitch, dout + off, pitch, (size_t)(hb - ha) * head_row,
+                                          (size_t)p.Sl, cudaMemcpyDeviceToHost, hp.d2h);
                 }
+                u += hb - ha;
             }
         }
     }

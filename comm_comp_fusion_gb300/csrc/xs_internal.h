@@ -61,8 +61,8 @@ inline size_t partial_record_bytes(int D) {
 // Chooses the grid and fills the schedule fields of p. With a workspace the
 // tail waves are balanced; without one every CTA takes whole items only.
 int attn_schedule(AttnParams &p, int num_sms, bool balanced);
-// Chunks of the host-buffer pipeline for this many (rank, batch) slices and input bytes.
-int host_chunks(int slices, long long input_bytes, int max_chunks);
+// Chunks of the host-buffer pipeline over (slice, head) units; fills bounds[0..n], returns n.
+int host_chunk_plan(int units, long long unit_bytes, long long min_bytes, int max_chunks, int *bounds);
 // Workspace bytes a balanced call needs (records, then counters), 256-aligned parts.
 size_t attn_workspace_bytes(int n_items, int n_kv, int D, int num_sms);
 

@@ -250,9 +250,11 @@ xs_status xs_attn_qkv8(const void *q8, const void *k8, const void *v8, void *out
  * The fused call (xs_attn_a2a_host) and attention only (xs_attn_host) on inputs
  * and output in HOST memory, for callers whose tensors live on the host. The X-Stage
  * paper has no counterpart; these calls exist for deployment. The copies are pipelined
- * with the compute: the P * B (rank, batch) slices of the inputs are split into up to
- * 16 chunks of at least about 8 MiB of inputs each (one chunk for small calls).
- * Chunk c's q, k, v slices are copied in on an internal stream, the caller's stream
+ * with the compute: the inputs' units, one head of one (rank, batch) slice each, are
+ * split in order into up to 16 chunks of at least 8 MiB of inputs each (one chunk
+ * for small calls), the first and the last the smallest. Chunk c's rows of q, k, v
+ * (whole slices, and the chunk's heads of every row of a partial slice at either
+ * end) are copied in on an internal stream, the caller's stream
  * runs the attention kernel over that chunk's work items, and an internal stream
  * copies the chunk's output out while later chunks are copied in and computed. For
  * xs_attn_a2a_host that output is the columns of the chunk's heads in the rows of its

@@ -1,5 +1,7 @@
 """The host-buffer calls (xs_attn_a2a_host, xs_attn_host): copies in, compute and
-copies out pipelined over chunks of (rank, batch) slices. Results must equal the device-buffer
+copies out pipelined over chunks of units, one head of one (rank, batch) slice each
+(a chunk: whole slices, and the same heads of every row of a partial slice at either
+end). Results must equal the device-buffer
 calls: bit for bit on the whole-item schedule, and within the parity bar (and
 against the oracle) on the balanced one, whose chunks split items differently."""
 import numpy as np
@@ -17,14 +19,15 @@ CASES = [
     (1, 1000, 4, 128, 2),    # ragged S
     (1, 512, 4, 256, 2),     # D = 256 (single-tile kernel)
 ]
-# large enough for several chunks (about 8 MiB of inputs each, at most one per (rank,
-# batch) slice, at most 16)
+# large enough for several chunks (at least 8 MiB of inputs each, sizes rising from the
+# first and falling towards the last, at most 16)
 MULTI = [
-    (1, 4096, 24, 128, 8),   # the DiT shape: 8 chunks, one rank each
-    (1, 8192, 32, 128, 32),  # 16 chunks of two ranks each
-    (1, 4032, 24, 128, 8),   # ragged S, 8 chunks
-    (2, 8192, 8, 128, 2),    # B = 2: 4 chunks of one (rank, batch) slice, so ranks are split
-    (3, 4096, 12, 64, 4),    # B = 3: 12 slices in 6 chunks of 2 (inputs 57 MB), chunks straddle ranks
+    (1, 4096, 24, 128, 8),   # the DiT shape: 8 chunks of one slice (3 heads)
+    (1, 8192, 32, 128, 32),  # 32 one-head slices in 9 chunks of 2 to 5
+    (1, 4032, 24, 128, 8),   # ragged S, 8 chunks of one slice
+    (2, 8192, 8, 128, 2),    # B = 2, 4 heads a slice: 8 chunks of half a slice
+    (3, 4096, 12, 64, 4),    # B = 3: 12 slices of 3 heads in 6 chunks of 2 slices, straddling ranks
+    (2, 8192, 16, 128, 2),   # 8 heads a slice, chunks of 2 to 5 heads, some across two slices
 ]
 
 
@@ -140,3 +143,23 @@ def test_host_call_rejects_device_memory_as_host_buffer():
     h = [torch.zeros(n, dtype=torch.int16).pin_memory() for _ in range(4)]
     st = xs.attn_a2a_host(d[4], h[1], h[2], h[3], d[0], d[1], d[2], d[3], B, S, H, D, P, 0.125, check=False)
     assert st == xs.XS_ERR_UNSUPPORTED and "q_host" in xs.last_error()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", MULTI[3:])
+def test_host_balanced_multi_chunk(case):
+    """The balanced schedule through the host path on shapes whose chunks split
+    slices by heads: within the parity bar of the device whole-item result."""
+    import torch
+    import comm_comp_fusion_gb300 as xs
+    B, S, H, D, P = case
+    scale = D ** -0.5
+    q, k, v = xsgen.random_inputs(53 + S + H + P, P, B, S, H, D)
+    ref_f = guarded(q.size)
+    xs.attn_a2a(to_dev(q), to_dev(k), to_dev(v), ref_f, B, S, H, D, P, scale)
+    torch.cuda.synchronize()
+    fused, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=True, pinned=True)
+    assert not (fused == SENTINEL).any()
+    ref = xsgen.bf16_bits_to_f32(from_dev(ref_f)).astype(np.float64)
+    assert_close(fused, ref, what=f"host balanced {case}")
+

@@ -27,8 +27,12 @@ int main() {
         xs::AttnParams p{};
         p.n_items = (int)items;
         p.n_kv = (int)nkv;
-        if (bal == 2) {  // host pipeline chunks: items = (rank, batch) slices, nkv = input bytes, sms = the cap
-            std::printf("%d\n", xs::host_chunks((int)items, nkv, sms));
+        if (bal == 2) {  // host pipeline chunks: items = units, nkv = input bytes per unit, sms = the cap
+            int b[65];
+            const int n = xs::host_chunk_plan((int)items, nkv, 8ll << 20, sms, b);
+            std::printf("%d", n);
+            for (int c = 0; c <= n; ++c) std::printf(" %d", b[c]);
+            std::printf("\n");
             continue;
         }
         const int g = xs::attn_schedule(p, sms, bal != 0);
@@ -118,18 +122,31 @@ def test_grid_rule_examples(schedule):
 
 
 def test_host_pipeline_chunks(schedule):
-    """One chunk per (rank, batch) slice, at most 16, and at least about 8 MiB of
-    inputs per chunk: DiT (8 slices, 75.5 MB of q, k, v) takes 8 chunks, a small
-    call one, 32 slices at S = 8192 the cap of 16. Chunk c's slices
-    [cn/k, (c+1)n/k) cover every slice once with at least one slice each."""
+    """Chunks of the host-buffer pipeline over (slice, head) units: they cover every
+    unit once, in order, at most 16 of them; the first and the last hold at least
+    8 MiB of inputs (or everything); sizes rise to the middle and fall after it.
+    Worked cases: the largest workload (8 slices of 10 heads, 12.6 MB of q, k, v per
+    head) starts and ends with one head; DiT (8 slices of 3 heads, 3.1 MB each)
+    keeps one slice per chunk; a small call is one chunk."""
     MB = 1 << 20
-    cases = [(8, 75497472, 16, 2), (4, 1 << 20, 16, 2), (32, 3 * 32 * 8192 * 128 * 2 * 4, 16, 2),
-             (8, 20 * MB, 16, 2), (1, 10 ** 9, 16, 2), (3, 0, 16, 2)]
-    got = [r[0] for r in schedule(cases)]
-    assert got == [8, 1, 16, 2, 1, 1]
-    for P in range(1, 40):
-        for inp in (0, 9 * MB, 40 * MB, 10 ** 9):
-            n = schedule([(P, inp, 16, 2)])[0][0]
-            assert 1 <= n <= min(P, 16)
-            spans = [((c + 1) * P // n) - (c * P // n) for c in range(n)]
-            assert sum(spans) == P and min(spans) >= 1
+    unit5 = 3 * 16384 * 128 * 2
+    cases = [(80, unit5, 16, 2), (24, 3 * 4096 * 128 * 2, 16, 2), (8, 3 * 256 * 64 * 2, 16, 2)]
+    got = schedule(cases)
+    sizes = [[b[i + 1] - b[i] for i in range(r[0])] for r in got for b in [r[1:]]]
+    assert sizes[0][0] == 1 and sizes[0][-1] == 1 and len(sizes[0]) <= 16
+    assert sizes[1] == [3] * 8
+    assert sizes[2] == [8]
+    for units in (1, 2, 3, 7, 24, 80, 257, 1000, 10000):
+        for ub in (1, 64 * 1024, 3 * MB, 13 * MB, 200 * MB):
+            for cap in (1, 2, 5, 16):
+                r = schedule([(units, ub, cap, 2)])[0]
+                n, b = r[0], list(r[1:])
+                what = (units, ub, cap, b)
+                assert 1 <= n <= cap and len(b) == n + 1, what
+                assert b[0] == 0 and b[-1] == units and all(x < y for x, y in zip(b, b[1:])), what
+                sz = [y - x for x, y in zip(b, b[1:])]
+                m = min(units, max(1, -(-(8 * MB) // ub)))
+                if n > 1:
+                    assert sz[0] >= m and sz[-1] >= m, what
+                top = sz.index(max(sz))
+                assert all(x <= y + 1 for x, y in zip(sz[:top], sz[1:top + 1])), what
