@@ -789,10 +789,18 @@ __global__ void __launch_bounds__(512, 1)
                 if (nseg == 1) tc_commit(BAR(BQ_EMPTY + 1));
                 for (int j = 0; j < nseg; ++j) {
                     const uint32_t vslot = kv_it % C::kSlots;
+                    const bool more = j + 1 < nseg, more0 = j + 1 < n0;
+                    // At D = 96, V_j and K_{j+1} (in long before they are needed) are waited
+                    // for together, so that P_0 V_j and S_0 go out as one group: 3.6%
+                    // faster there, about 1% slower at D = 64 and 128 (measured on GB300,
+                    // builds alternated), where K_{j+1} is waited for between the two.
+                    constexpr bool kEarlyK = D == 96;
                     ok = bwait(BAR(BKV_FULL + vslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
+                    if (kEarlyK && ok && more)
+                        ok = bwait(BAR(BKV_FULL + (kv_it + 1) % C::kSlots), ((kv_it + 1) / C::kSlots) & 1u, abort_flag,
+                                   kSiteMmaKV);
                     if (!ok) break;
                     ++kv_it;
-                    const bool more = j + 1 < nseg, more0 = j + 1 < n0;
                     // ---- tile 0: O0 += P0 V_j, then S0 for the next K/V tile
                     if (!CAU || j < n0) {
                         ok = bwait(BAR(BP_FULL + 0), pph0, abort_flag, kSiteMmaP);
@@ -807,8 +815,10 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     if (more) {
                         kslot = kv_it % C::kSlots;
-                        ok = bwait(BAR(BKV_FULL + kslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
-                        if (!ok) break;
+                        if (!kEarlyK) {
+                            ok = bwait(BAR(BKV_FULL + kslot), (kv_it / C::kSlots) & 1u, abort_flag, kSiteMmaKV);
+                            if (!ok) break;
+                        }
                         ++kv_it;
                         if (more0) {
                             issue_S(0, kslot);
