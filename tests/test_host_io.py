@@ -134,6 +134,24 @@ def test_host_dit_full_size_sampled():
 
 
 @pytest.mark.gpu
+def test_host_largest_workload_tile_rows():
+    """The largest workload (B = 2, S = 16384, H = 40, P = 4: 10 heads a slice) through
+    the host path with the balanced schedule, as the bench's end-to-end line runs it:
+    its chunks start and end with one head and split slices by heads. One row of every
+    (rank, batch, head, query tile) against the oracle."""
+    from xs_testlib import tile_rows, seq_rows_of
+    w = xsgen.WORKLOADS[4]
+    B, S, H, D, P, scale = w["B"], w["S"], w["H"], w["D"], w["P"], w["scale"]
+    q, k, v = xsgen.workload_inputs(4)
+    fused, _, _ = _run(q, k, v, B, S, H, D, P, scale, balanced=True, pinned=True)
+    assert not (fused == SENTINEL).any()
+    rows = tile_rows(B, S, H, P, 1, seed=41)
+    ref = oracle.attention_rows(q, k, v, B, S, H, D, P, scale, rows)
+    got = fused.reshape(-1, D)[seq_rows_of(rows, B, S, H, D, P)]
+    assert_close(got.ravel(), ref.ravel(), what="host largest workload, one row per tile")
+
+
+@pytest.mark.gpu
 def test_host_call_rejects_device_memory_as_host_buffer():
     import torch
     import comm_comp_fusion_gb300 as xs
